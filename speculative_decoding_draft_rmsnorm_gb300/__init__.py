@@ -1,0 +1,180 @@
+"""GB300 (sm_103a) DFlash draft block attention: Python binding of libdflash_gb300.so.
+
+The binding only marshals arguments: every step of the path (context-K norm+RoPE, the
+fused q/k prologue, block attention, split-KV combine) runs in the library's CUDA
+kernels. PyTorch supplies device memory and the current stream. There is no CPU or
+PyTorch fallback: if the library cannot be built or loaded, every call raises.
+
+Entry points mirror include/dflash.h:
+    context_kv(...)          -> dflash_context_kv
+    block_attention(...)     -> dflash_block_attention
+    workspace_size(...)      -> dflash_block_attention_workspace_size
+    check_error(workspace)   -> dflash_check_error
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+__all__ = ["load", "lib_path", "context_kv", "block_attention", "workspace_size", "alloc_workspace",
+           "check_error", "DFlashError", "OUT_BF16", "OUT_F32", "FLAG_FORCE_SPLIT", "FLAG_NO_SPLIT",
+           "ERR_INVALID_ARG", "ERR_UNSUPPORTED", "ERR_WORKSPACE", "ERR_CUDA", "ERR_DEVICE_TIMEOUT",
+           "ERR_DEVICE_METADATA"]
+
+OUT_BF16, OUT_F32 = 0, 1
+FLAG_FORCE_SPLIT, FLAG_NO_SPLIT = 1, 2
+ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_WORKSPACE, ERR_CUDA, ERR_DEVICE_TIMEOUT, ERR_DEVICE_METADATA = \
+    -1, -2, -3, -4, -5, -6
+
+_lock = threading.Lock()
+_lib = None
+
+
+class DFlashError(RuntimeError):
+    def __init__(self, code: int, message: str):
+        super().__init__(f"dflash error {code}: {message}")
+        self.code = code
+
+
+def lib_path() -> str:
+    from . import _build
+    return _build.LIB_PATH
+
+
+def load(build_if_missing: bool = True):
+    """Loads the library (building it in-tree with nvcc first if it is missing)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        from . import _build
+        if not _build.up_to_date():
+            if not build_if_missing:
+                raise RuntimeError(f"{_build.LIB_PATH} is not built; run __graft_entry__.build()")
+            _build.build()
+        lib = ctypes.CDLL(_build.LIB_PATH)
+        P, I32, I64, F32, SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
+        lib.dflash_last_error.restype = ctypes.c_char_p
+        lib.dflash_last_error.argtypes = []
+        lib.dflash_version.restype = I32
+        lib.dflash_version.argtypes = []
+        lib.dflash_context_kv.restype = I32
+        lib.dflash_context_kv.argtypes = [P, P, P, P, P, I64, I32, I32, F32, F32, P, P, I64, P]
+        lib.dflash_block_attention_workspace_size.restype = SZ
+        lib.dflash_block_attention_workspace_size.argtypes = [I32, I64, I32, I32, I32, I64, I32, I32, I32, I32, I32, I32]
+        lib.dflash_block_attention.restype = I32
+        lib.dflash_block_attention.argtypes = ([P] * 11 + [I32, I64, I32, I32, I32, I64, I32, I32, F32, F32, F32,
+                                                           I32, I32, I32, P, P, SZ, I32, P])
+        lib.dflash_check_error.restype = I32
+        lib.dflash_check_error.argtypes = [P, P]
+        _lib = lib
+        return lib
+
+
+def _raise(rc: int) -> None:
+    if rc != 0:
+        raise DFlashError(rc, load().dflash_last_error().decode(errors="replace"))
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _check_tensor(name, t, dtype, shape=None):
+    import torch
+    if t is None:
+        return
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must live on a CUDA device")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+
+
+def context_kv(k_raw, ctx_pos, k_norm_w, ctx_k, *, v=None, ctx_v=None, slot=None, eps=1e-6, theta=1e6,
+               stream=None) -> None:
+    """Writes rope(rmsnorm(k_raw)) into ctx_k (and v into ctx_v) at rows `slot` (or 0..n-1)."""
+    import torch
+    n, hkv, dh = k_raw.shape
+    _check_tensor("k_raw", k_raw, torch.bfloat16)
+    _check_tensor("v", v, torch.bfloat16, (n, hkv, dh))
+    _check_tensor("ctx_pos", ctx_pos, torch.int32, (n,))
+    _check_tensor("k_norm_w", k_norm_w, torch.bfloat16, (dh,))
+    _check_tensor("slot", slot, torch.int32, (n,))
+    _check_tensor("ctx_k", ctx_k, torch.bfloat16)
+    _check_tensor("ctx_v", ctx_v, torch.bfloat16, None if ctx_v is None else tuple(ctx_k.shape))
+    if tuple(ctx_k.shape[1:]) != (hkv, dh):
+        raise ValueError("ctx_k must be [capacity, Hkv, Dh]")
+    rc = load().dflash_context_kv(_ptr(k_raw), _ptr(v), _ptr(ctx_pos), _ptr(k_norm_w), _ptr(slot), n, hkv, dh,
+                                  float(eps), float(theta), _ptr(ctx_k), _ptr(ctx_v), ctx_k.shape[0], _stream(stream))
+    _raise(rc)
+
+
+def workspace_size(num_reqs, total_q, hq, hkv, dh, total_ctx, max_ctx_len, max_block_len, causal=False, window=0,
+                   out_dtype=OUT_BF16, flags=0) -> int:
+    n = load().dflash_block_attention_workspace_size(num_reqs, total_q, hq, hkv, dh, total_ctx, max_ctx_len,
+                                                     max_block_len, int(causal), int(window), out_dtype, flags)
+    if n == 0:
+        _raise(ERR_INVALID_ARG)
+    return int(n)
+
+
+def alloc_workspace(nbytes: int, device=None):
+    import torch
+    return torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device or "cuda")
+
+
+def block_attention(q, k_blk, v_blk, ctx_k, ctx_v, query_start_loc, ctx_start_loc, ctx_lens, positions, q_norm_w,
+                    k_norm_w, *, max_ctx_len, max_block_len, out=None, workspace=None, eps=1e-6, theta=1e6,
+                    scale=0.0, causal=False, window=0, out_dtype=OUT_BF16, flags=0, stream=None):
+    """Block attention of every block row over [context ; block] of its request.
+
+    Shapes: q [T, Hq, Dh], k_blk / v_blk [T, Hkv, Dh], ctx_k / ctx_v [total_ctx, Hkv, Dh] (bf16);
+    query_start_loc / ctx_start_loc [N+1], ctx_lens [N], positions [T] (int32).
+    Returns `out` [T, Hq, Dh] (bf16, or f32 with out_dtype=OUT_F32).
+    """
+    import torch
+    t, hq, dh = q.shape
+    hkv = k_blk.shape[1]
+    n = query_start_loc.shape[0] - 1
+    total_ctx = ctx_k.shape[0]
+    for name, ten, shp in [("q", q, None), ("k_blk", k_blk, (t, hkv, dh)), ("v_blk", v_blk, (t, hkv, dh)),
+                           ("ctx_k", ctx_k, (total_ctx, hkv, dh)), ("ctx_v", ctx_v, (total_ctx, hkv, dh)),
+                           ("q_norm_w", q_norm_w, (dh,)), ("k_norm_w", k_norm_w, (dh,))]:
+        _check_tensor(name, ten, torch.bfloat16, shp)
+    for name, ten, shp in [("query_start_loc", query_start_loc, (n + 1,)), ("ctx_start_loc", ctx_start_loc, (n + 1,)),
+                           ("ctx_lens", ctx_lens, (n,)), ("positions", positions, (t,))]:
+        _check_tensor(name, ten, torch.int32, shp)
+    odt = torch.float32 if out_dtype == OUT_F32 else torch.bfloat16
+    if out is None:
+        out = torch.empty((t, hq, dh), dtype=odt, device=q.device)
+    _check_tensor("out", out, odt, (t, hq, dh))
+    need = workspace_size(n, t, hq, hkv, dh, total_ctx, max_ctx_len, max_block_len, causal, window, out_dtype, flags)
+    if workspace is None:
+        workspace = alloc_workspace(need, q.device)
+    _check_tensor("workspace", workspace, torch.uint8)
+    rc = load().dflash_block_attention(
+        _ptr(q), _ptr(k_blk), _ptr(v_blk), _ptr(ctx_k), _ptr(ctx_v), _ptr(query_start_loc), _ptr(ctx_start_loc),
+        _ptr(ctx_lens), _ptr(positions), _ptr(q_norm_w), _ptr(k_norm_w), n, t, hq, hkv, dh, total_ctx,
+        int(max_ctx_len), int(max_block_len), float(eps), float(theta), float(scale), int(causal), int(window),
+        out_dtype, _ptr(out), _ptr(workspace), workspace.numel(), flags, _stream(stream))
+    _raise(rc)
+    return out
+
+
+def check_error(workspace, stream=None) -> None:
+    """Raises DFlashError if the last attention call on `workspace` recorded a device error."""
+    _raise(load().dflash_check_error(_ptr(workspace), _stream(stream)))

@@ -1,0 +1,41 @@
+// norm_rope.cu -- host helpers and the stand-alone launch of the fused per-head
+// RMSNorm + NeoX RoPE kernel (used for the context K/V store write).
+#include <cmath>
+
+#include "norm_rope.cuh"
+
+namespace dflash {
+
+void make_rope_turns(int dh, double theta, RopeTurns* out) {
+  const double two_pi = 6.283185307179586476925286766559;
+  for (int i = 0; i < kMaxHeadDim / 2; ++i) {
+    double g = 0.0;
+    if (i < dh / 2) g = std::pow(theta, -2.0 * i / dh) / two_pi;
+    const float hi = static_cast<float>(g);
+    out->hi[i] = hi;
+    out->lo[i] = static_cast<float>(g - static_cast<double>(hi));
+  }
+}
+
+template <int DH>
+__global__ void __launch_bounds__(256) norm_rope_kernel(const __grid_constant__ NormRopeJob job) {
+  const int64_t warp_id = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int64_t n_warps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+  norm_rope_rows<DH>(job, warp_id, n_warps);
+}
+
+cudaError_t launch_norm_rope(const NormRopeJob& job, int dh, int num_sms, cudaStream_t stream) {
+  if (job.n_tok <= 0) return cudaSuccess;
+  const int64_t warps_needed = job.n_tok;
+  int64_t blocks = (warps_needed + 7) / 8;
+  const int64_t cap = static_cast<int64_t>(num_sms) * 8;  // 8 blocks x 8 warps resident per SM
+  if (blocks > cap) blocks = cap;
+  if (dh == 128) {
+    norm_rope_kernel<128><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(job);
+  } else {
+    norm_rope_kernel<64><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(job);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace dflash
