@@ -1,0 +1,471 @@
+#!/usr/bin/env python3
+"""Benchmark of the DFlash draft block-attention hot path on GB300.
+
+One step = one pass of the whole path over one synthetic batch, as a draft step runs it:
+  1. dflash_context_kv: the rows appended to each request's context this step (the
+     previous block, B rows per request) are normed, rotated and scattered into the
+     device-resident context K/V store;
+  2. dflash_block_attention: q/k norm + RoPE prologue, block attention of every block
+     row over [context ; block] of its request, split-KV combine.
+The context store is device state that persists across steps (it is built once,
+untimed), as the draft model keeps it resident.
+
+Metric: K/V HBM GB/s of block attention (algorithmic bytes: each allowed context or
+block key's K and V read once per (request, kv head)), with TFLOP/s and the fraction
+of the GB300 roofline beside it. L2 is flushed (256 MB write) before every step,
+outside the timed events.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from speculative_decoding_draft_rmsnorm_gb300 import workloads as W  # noqa: E402
+
+METRIC = "DFlash block-attn TFLOP/s and K/V HBM GB/s, % of GB300 roofline"
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+
+
+# ---------------------------------------------------------------- accounting
+def algorithmic_counts(cfg: W.Config, ctx_lens, block_lens) -> dict:
+    """Keys each (request, kv head) must read, allowed (query, key) pairs, bytes and flops.
+
+    A key counts once per (request, kv head) if some block row of the request may attend
+    to it (window-masked context keys are not counted). Bytes: bf16 K and V of those
+    keys. Flops: 4 * Dh per allowed (query row, key) pair and query head (QK^T and PV).
+    """
+    keys = 0
+    pairs = 0
+    for c, b in zip(ctx_lens, block_lens):
+        c, b = int(c), int(b)
+        if b == 0:
+            continue
+        if not cfg.causal:
+            keys += c + b
+            pairs += b * (c + b)
+            continue
+        w = cfg.window if cfg.window > 0 else c + b + 1
+        keys += (c + b) - max(0, c - w + 1)
+        for i in range(c, c + b):
+            pairs += i + 1 - max(0, i - w + 1)
+    return {"keys": keys, "pairs": pairs, "kv_bytes": keys * cfg.hkv * cfg.dh * 4,
+            "flops": 4 * cfg.dh * pairs * cfg.hq}
+
+
+def describe(cfg: W.Config, ctx_lens) -> dict:
+    mask = "bidirectional" if not cfg.causal else (f"causal, window {cfg.window}" if cfg.window else "causal")
+    if cfg.ctx_len is not None:
+        c = str(cfg.ctx_len)
+    elif cfg.ctx_uniform is not None:
+        c = f"U[{cfg.ctx_uniform[0]},{cfg.ctx_uniform[1]}] (sum {int(sum(ctx_lens))})"
+    else:
+        c = f"log-uniform[{cfg.ctx_loguniform[0]},{cfg.ctx_loguniform[1]}] (sum {int(sum(ctx_lens))})"
+    return {"workload": cfg.name + ": " + cfg.note, "requests": cfg.num_reqs, "ctx_len": c, "block": cfg.block,
+            "hq": cfg.hq, "hkv": cfg.hkv, "dh": cfg.dh, "mask": mask, "seed": cfg.seed,
+            "appended_rows_per_request": cfg.block,
+            "l2": "flushed before every step (256 MB write, outside the timed events)"}
+
+
+def load_peaks() -> tuple[dict, str]:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"])}, "of measured"
+    except Exception:
+        return {"hbm_gbs": FALLBACK_HBM_GBS, "bf16_tflops": FALLBACK_BF16_TFLOPS}, "of fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "speculative_decoding_draft_rmsnorm_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per launch from the committed ncu capture, if the kernels are unchanged."""
+    p = os.path.join(ROOT, "profiles", "attention_traffic.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        if d.get("source_hash") != kernel_source_hash():
+            return None
+        return d.get("per_launch_bytes", {}).get(workload)
+    except Exception:
+        return None
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.proc = None
+        self.dev = device_index
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(device_index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            return None
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- GPU arm
+class Step:
+    """Device-resident inputs of one step and the two library calls that make it."""
+
+    def __init__(self, lib, b: W.Batch, flags: int):
+        import numpy as np
+        import torch
+        self.lib, self.b, self.cfg, self.flags = lib, b, b.cfg, flags
+        c = b.cfg
+
+        def d16(a):
+            return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).cuda()
+
+        def d32(a):
+            return torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).cuda()
+
+        self.d16, self.d32 = d16, d32
+        # rows appended this step: the last min(B, C) context rows of every request
+        idx = []
+        for r in range(c.num_reqs):
+            a = min(int(b.block_lens[r]), int(b.ctx_lens[r]))
+            end = int(b.ctx_start_loc[r]) + int(b.ctx_lens[r])
+            idx.extend(range(end - a, end))
+        self.new_idx = np.array(idx, dtype=np.int64)
+        self.host = {
+            "k_new": np.ascontiguousarray(b.ctx_k_raw[self.new_idx]),
+            "v_new": np.ascontiguousarray(b.ctx_v[self.new_idx]),
+            "pos_new": np.ascontiguousarray(b.ctx_pos[self.new_idx]).astype(np.int32),
+            "slot": self.new_idx.astype(np.int32),
+            "q": b.q, "k_blk": b.k_blk, "v_blk": b.v_blk, "positions": b.positions,
+            "qsl": b.query_start_loc, "csl": b.ctx_start_loc, "clen": b.ctx_lens,
+        }
+        self.dev = {k: (d16(v) if v.dtype == np.uint16 else d32(v)) for k, v in self.host.items()}
+        self.q_norm_w, self.k_norm_w = d16(b.q_norm_w), d16(b.k_norm_w)
+        # the resident context store, built once (untimed)
+        self.ctx_k = torch.empty(b.ctx_k_raw.shape, dtype=torch.bfloat16, device="cuda")
+        self.ctx_v = d16(b.ctx_v)
+        lib.context_kv(d16(b.ctx_k_raw), d32(b.ctx_pos), self.k_norm_w, self.ctx_k, eps=c.eps, theta=c.theta)
+        self.max_ctx = int(max(1, b.ctx_lens.max(initial=0)))
+        self.max_blk = int(max(1, b.block_lens.max(initial=0)))
+        t, hq, dh = b.q.shape
+        self.out = torch.empty((t, hq, dh), dtype=torch.bfloat16, device="cuda")
+        self.args = (b.cfg.num_reqs, t, hq, c.hkv, dh, b.ctx_k_raw.shape[0], self.max_ctx, self.max_blk, c.causal,
+                     c.window, lib.OUT_BF16, flags)
+        self.plan = lib.plan(*self.args)
+        self.ws = lib.alloc_workspace(lib.workspace_size(*self.args))
+        torch.cuda.synchronize()
+
+    def append(self, dev=None):
+        d = dev or self.dev
+        c = self.cfg
+        self.lib.context_kv(d["k_new"], d["pos_new"], self.k_norm_w, self.ctx_k, v=d["v_new"], ctx_v=self.ctx_v,
+                            slot=d["slot"], eps=c.eps, theta=c.theta)
+
+    def attend(self, dev=None):
+        d = dev or self.dev
+        c = self.cfg
+        self.lib.block_attention(d["q"], d["k_blk"], d["v_blk"], self.ctx_k, self.ctx_v, d["qsl"], d["csl"],
+                                 d["clen"], d["positions"], self.q_norm_w, self.k_norm_w, max_ctx_len=self.max_ctx,
+                                 max_block_len=self.max_blk, out=self.out, workspace=self.ws, eps=c.eps,
+                                 theta=c.theta, causal=c.causal, window=c.window, flags=self.flags)
+
+    def launches_per_step(self) -> int:
+        return 1 + int(self.plan["launches"])
+
+
+def run_gpu(args, b: W.Batch, rank: int, world: int) -> dict | None:
+    import numpy as np
+    import torch
+    import speculative_decoding_draft_rmsnorm_gb300 as lib
+
+    lib.load(build_if_missing=False)
+    dev_index = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(dev_index)
+    cfg = b.cfg
+    flags = lib.FLAG_FORCE_SPLIT if cfg.force_split else 0
+    st = Step(lib, b, flags)
+    counts = algorithmic_counts(cfg, b.ctx_lens, b.block_lens)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    # ---- warm-up
+    for _ in range(args.warmup):
+        flush.zero_()
+        st.append()
+        st.attend()
+    torch.cuda.synchronize()
+    barrier()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(dev_index)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    for i in range(args.steps):
+        flush.zero_()
+        ev[i][0].record(stream)
+        st.append()
+        ev[i][1].record(stream)
+        st.attend()
+        ev[i][2].record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    lib.check_error(st.ws)
+    step_ms = [e[0].elapsed_time(e[2]) for e in ev]
+    attn_ms = [e[1].elapsed_time(e[2]) for e in ev]
+    total_ms = sum(step_ms)
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([total_ms], dtype=torch.float64, device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+
+    # ---- end to end through the public API with host buffers (pinned), copies timed
+    pinned = {k: torch.from_numpy(np.ascontiguousarray(v).view(np.int16) if v.dtype == np.uint16 else
+                                  np.ascontiguousarray(v)).pin_memory() for k, v in st.host.items()}
+    dev_in = {k: torch.empty(v.shape, dtype=v.dtype, device="cuda") for k, v in pinned.items()}
+    out_host = torch.empty(st.out.shape, dtype=torch.bfloat16).pin_memory()
+    h2d = sum(v.numel() * v.element_size() for v in pinned.values())
+    d2h = out_host.numel() * out_host.element_size()
+
+    def e2e_step():
+        for k, v in pinned.items():
+            dev_in[k].copy_(v, non_blocking=True)
+        dv = {k: (v.view(torch.bfloat16) if v.dtype == torch.int16 else v) for k, v in dev_in.items()}
+        st.append(dv)
+        st.attend(dv)
+        out_host.copy_(st.out, non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        flush.zero_()
+        e2e_step()
+    torch.cuda.synchronize()
+    eev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+    for i in range(args.steps):
+        flush.zero_()
+        eev[i][0].record(stream)
+        e2e_step()
+        eev[i][1].record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = sum(e[0].elapsed_time(e[1]) for e in eev)
+
+    peaks, peak_note = load_peaks()
+    attn_avg_s = statistics.mean(attn_ms) / 1e3
+    achieved = counts["kv_bytes"] / attn_avg_s / 1e9
+    res = {
+        "metric": METRIC,
+        "value": world * counts["kv_bytes"] * args.steps / (total_ms / 1e3) / 1e9,
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": total_ms / args.steps,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": {**describe(cfg, b.ctx_lens), "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"},
+        "tflops": world * counts["flops"] * args.steps / (total_ms / 1e3) / 1e12,
+        "attention_ms": statistics.mean(attn_ms),
+        "append_ms": statistics.mean(s - a for s, a in zip(step_ms, attn_ms)),
+        "roofline": {
+            "bound": "hbm",
+            "kernel": "dflash_block_attention call (prologue + attention + combine launches)",
+            "achieved": achieved,
+            "peak": peaks["hbm_gbs"],
+            "unit": "GB/s",
+            "frac": achieved / peaks["hbm_gbs"],
+            "peak_source": peak_note,
+            "traffic": recorded_traffic(cfg.name),
+            "algorithmic_bytes_per_launch": counts["kv_bytes"],
+            "tensor_tflops": counts["flops"] / attn_avg_s / 1e12,
+            "tensor_frac": counts["flops"] / attn_avg_s / 1e12 / peaks["bf16_tflops"],
+        },
+        "e2e": {"value": world * counts["kv_bytes"] * args.steps / (e2e_ms / 1e3) / 1e9, "unit": "GB/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": st.launches_per_step() * args.steps,
+        "clocks": clk,
+        "plan": st.plan,
+    }
+    return res
+
+
+# ---------------------------------------------------------------- oracle (CPU)
+def oracle_sample(b_full: W.Batch, budget_s: float):
+    """Times the f64 oracle on a bounded prefix of the workload's requests.
+
+    Returns (seconds, kv_bytes of the sample, description, cores). The context store
+    of the sample is built by the oracle first (untimed); the timed part is the step:
+    the appended rows' store write plus block attention.
+    """
+    import numpy as np
+    import oracle
+
+    def sub_batch(b: W.Batch, k: int) -> W.Batch:
+        q1, c1 = int(b.query_start_loc[k]), int(b.ctx_start_loc[k])
+        return W.Batch(cfg=b.cfg, ctx_lens=b.ctx_lens[:k], block_lens=b.block_lens[:k],
+                       query_start_loc=b.query_start_loc[:k + 1], ctx_start_loc=b.ctx_start_loc[:k + 1],
+                       positions=b.positions[:q1], ctx_pos=b.ctx_pos[:c1], q=b.q[:q1], k_blk=b.k_blk[:q1],
+                       v_blk=b.v_blk[:q1], ctx_k_raw=b.ctx_k_raw[:c1], ctx_v=b.ctx_v[:c1], q_norm_w=b.q_norm_w,
+                       k_norm_w=b.k_norm_w)
+
+    cfg = b_full.cfg
+    lens = b_full.ctx_lens.astype(np.int64)
+
+    def time_step(sb: W.Batch) -> float:
+        c = sb.cfg
+        _, store = oracle.context_kv(sb.ctx_k_raw, sb.ctx_pos, sb.k_norm_w, c.eps, c.theta)
+        idx = []
+        for r in range(len(sb.ctx_lens)):
+            a = min(int(sb.block_lens[r]), int(sb.ctx_lens[r]))
+            end = int(sb.ctx_start_loc[r]) + int(sb.ctx_lens[r])
+            idx.extend(range(end - a, end))
+        idx = np.array(idx, dtype=np.int64)
+        t0 = time.perf_counter()
+        _, new16 = oracle.context_kv(sb.ctx_k_raw[idx], sb.ctx_pos[idx], sb.k_norm_w, c.eps, c.theta)
+        store[idx] = new16
+        oracle.block_attention(sb.q, sb.k_blk, sb.v_blk, store, sb.ctx_v, sb.query_start_loc, sb.ctx_start_loc,
+                               sb.ctx_lens, sb.positions, sb.q_norm_w, sb.k_norm_w, eps=c.eps, theta=c.theta,
+                               causal=c.causal, window=c.window)
+        return time.perf_counter() - t0
+
+    t1 = time_step(sub_batch(b_full, 1))
+    k = int(max(1, min(cfg.num_reqs, math.floor(budget_s / max(t1, 1e-3)))))
+    sb = sub_batch(b_full, k)
+    secs = time_step(sb) if k > 1 else t1
+    cnt = algorithmic_counts(cfg, sb.ctx_lens, sb.block_lens)
+    desc = f"first {k} of {cfg.num_reqs} requests (context lengths {int(lens[:k].sum())} rows in all)"
+    return secs, cnt["kv_bytes"], desc, oracle.num_threads(), sb, time_step
+
+
+def cpu_baseline(b: W.Batch) -> dict:
+    secs, nbytes, desc, cores, _, _ = oracle_sample(b, budget_s=12.0)
+    return {"value": nbytes / secs / 1e9, "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": desc,
+            "seconds": secs}
+
+
+def run_reference(args, b: W.Batch) -> dict:
+    # each step: the oracle on a bounded sample sized so that the whole run takes minutes
+    cfg = b.cfg
+    per_step_budget = max(0.5, 150.0 / max(1, args.steps + args.warmup))
+    secs, nbytes, desc, cores, sb, time_step = oracle_sample(b, per_step_budget)
+    for _ in range(max(0, args.warmup - 1)):
+        time_step(sb)
+    times = [time_step(sb) for _ in range(args.steps)]
+    total = sum(times)
+    value = nbytes * args.steps / total / 1e9
+    return {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": value,
+        "unit": "GB/s",
+        "n_gpus": int(os.environ.get("WORLD_SIZE", "1")),
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": total / args.steps * 1e3,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic",
+        "config": describe(cfg, b.ctx_lens),
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": desc},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main() -> int:
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="qwen3_4b", choices=sorted(W.CONFIGS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    cfg = W.CONFIGS[args.workload]
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args, W.make_batch(cfg))), flush=True)
+        return 0
+
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+        dist.init_process_group("nccl")
+    b = W.make_batch(cfg)
+    res = run_gpu(args, b, rank, world)
+    if rank == 0:
+        if not args.no_cpu_baseline:
+            res["cpu_baseline"] = cpu_baseline(b)
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -107,6 +107,17 @@ DFLASH_API size_t dflash_block_attention_workspace_size(int num_reqs, int64_t to
                                                         int causal, int window, int out_dtype, int flags);
 
 /*
+ * Describes how dflash_block_attention would run with these arguments on the current
+ * device: plan[0] = kernel launches per call (prologue, attention and, when a request's
+ * keys may be split over several CTAs, the combine pass), plan[1] = key tiles (128 keys)
+ * per split, plan[2] = upper bound of work units, plan[3] = attention CTAs, plan[4] =
+ * workspace bytes / 256 (rounded up). Returns DFLASH_OK or an error status.
+ */
+DFLASH_API int dflash_block_attention_plan(int num_reqs, int64_t total_q, int hq, int hkv, int dh, int64_t total_ctx,
+                                           int max_ctx_len, int max_block_len, int causal, int window, int out_dtype,
+                                           int flags, int64_t plan[5]);
+
+/*
  * dflash_block_attention -- attention of every block row over [context ; block] of its
  * request, with the q/k RMSNorm + NeoX RoPE prologue fused in.
  * (qwen3_dflash.cpp: ForwardWithCtxKVDev builds per request the combined sequence

@@ -17,7 +17,7 @@ import ctypes
 import os
 import threading
 
-__all__ = ["load", "lib_path", "context_kv", "block_attention", "workspace_size", "alloc_workspace",
+__all__ = ["load", "lib_path", "context_kv", "block_attention", "workspace_size", "plan", "alloc_workspace",
            "check_error", "DFlashError", "OUT_BF16", "OUT_F32", "FLAG_FORCE_SPLIT", "FLAG_NO_SPLIT",
            "ERR_INVALID_ARG", "ERR_UNSUPPORTED", "ERR_WORKSPACE", "ERR_CUDA", "ERR_DEVICE_TIMEOUT",
            "ERR_DEVICE_METADATA"]
@@ -66,6 +66,8 @@ def load(build_if_missing: bool = True):
         lib.dflash_block_attention.restype = I32
         lib.dflash_block_attention.argtypes = ([P] * 11 + [I32, I64, I32, I32, I32, I64, I32, I32, F32, F32, F32,
                                                            I32, I32, I32, P, P, SZ, I32, P])
+        lib.dflash_block_attention_plan.restype = I32
+        lib.dflash_block_attention_plan.argtypes = [I32, I64, I32, I32, I32, I64, I32, I32, I32, I32, I32, I32, P]
         lib.dflash_check_error.restype = I32
         lib.dflash_check_error.argtypes = [P, P]
         _lib = lib
@@ -130,6 +132,16 @@ def workspace_size(num_reqs, total_q, hq, hkv, dh, total_ctx, max_ctx_len, max_b
     if n == 0:
         _raise(ERR_INVALID_ARG)
     return int(n)
+
+
+def plan(num_reqs, total_q, hq, hkv, dh, total_ctx, max_ctx_len, max_block_len, causal=False, window=0,
+         out_dtype=OUT_BF16, flags=0) -> dict:
+    """How a call with these arguments runs: launches, tiles per split, unit bound, CTAs."""
+    arr = (ctypes.c_int64 * 5)()
+    _raise(load().dflash_block_attention_plan(num_reqs, total_q, hq, hkv, dh, total_ctx, max_ctx_len, max_block_len,
+                                              int(causal), int(window), out_dtype, flags, arr))
+    return {"launches": arr[0], "tiles_per_split": arr[1], "units_max": arr[2], "ctas": arr[3],
+            "workspace_bytes": arr[4] * 256}
 
 
 def alloc_workspace(nbytes: int, device=None):

@@ -2,6 +2,7 @@
 // validation, workspace carve-up and kernel launches. No entry point allocates,
 // synchronises (except dflash_check_error, which reads the device error word) or
 // throws.
+#include <algorithm>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -99,7 +100,7 @@ int dflash_context_kv(const dflash_bf16* k_raw, const dflash_bf16* v, const int3
     return fail(DFLASH_ERR_INVALID_ARG, "null tensor pointer");
   if (!aligned16(k_raw) || !aligned16(ctx_k) || !aligned16(k_norm_w) || (v && (!aligned16(v) || !aligned16(ctx_v))))
     return fail(DFLASH_ERR_INVALID_ARG, "tensor pointers must be 16-byte aligned");
-  if (slot && v == ctx_v) return fail(DFLASH_ERR_INVALID_ARG, "v may not alias ctx_v when slots are given");
+  if (slot && v && v == ctx_v) return fail(DFLASH_ERR_INVALID_ARG, "v may not alias ctx_v when slots are given");
   if (slot && k_raw == ctx_k) return fail(DFLASH_ERR_INVALID_ARG, "k_raw may not alias ctx_k when slots are given");
   int sms = 0;
   int rc = device_sms(&sms);
@@ -135,6 +136,29 @@ size_t dflash_block_attention_workspace_size(int num_reqs, int64_t total_q, int 
                                                          flags, sms);
   ok();
   return w.total;
+}
+
+int dflash_block_attention_plan(int num_reqs, int64_t total_q, int hq, int hkv, int dh, int64_t total_ctx,
+                                int max_ctx_len, int max_block_len, int causal, int window, int out_dtype, int flags,
+                                int64_t plan[5]) {
+  int rc = check_sizes(num_reqs, total_q, hq, hkv, dh, total_ctx, max_ctx_len, max_block_len, out_dtype);
+  if (rc != DFLASH_OK) return rc;
+  if (!plan) return fail(DFLASH_ERR_INVALID_ARG, "null plan array");
+  if (causal != 0 && causal != 1) return fail(DFLASH_ERR_INVALID_ARG, "causal must be 0 or 1");
+  if (window < 0 || (window > 0 && !causal)) return fail(DFLASH_ERR_INVALID_ARG, "window needs causal=1");
+  int sms = 0;
+  rc = device_sms(&sms);
+  if (rc != DFLASH_OK) return rc;
+  const dflash::WorkspacePlan w = dflash::plan_workspace(num_reqs, total_q, hq, hkv, dh, total_ctx, max_ctx_len,
+                                                         max_block_len, window, causal, out_dtype == DFLASH_OUT_F32,
+                                                         flags, sms);
+  const bool any = num_reqs > 0 && total_q > 0;
+  plan[0] = any ? (w.may_split ? 3 : 2) : 0;
+  plan[1] = w.tiles_per_split;
+  plan[2] = w.units_max;
+  plan[3] = any ? std::max(1, std::min(sms, w.units_max)) : 0;
+  plan[4] = static_cast<int64_t>((w.total + 255) / 256);
+  return ok();
 }
 
 int dflash_block_attention(const dflash_bf16* q_raw, const dflash_bf16* k_blk, const dflash_bf16* v_blk,

@@ -35,8 +35,11 @@ def test_context_kv_matches_oracle(hkv, dh, n):
     D().context_kv(U.bf16_dev(b.ctx_k_raw), U.i32_dev(pos), U.bf16_dev(b.k_norm_w), out, eps=c.eps, theta=c.theta)
     got_bits = U.dev_bits(out).reshape(exact.shape)
     got = W.bf16_to_f64(got_bits).reshape(exact.shape)
+    # one bf16 ulp of the exact value, plus the absolute error of the f32 rotation of
+    # normalised values (|x^| < ~8): where cos/sin terms cancel, the result is tiny and
+    # its own ulp is smaller than that f32 error
     ulp = 2.0 ** (np.floor(np.log2(np.maximum(np.abs(exact), 1e-30))) - 7)
-    assert np.all(np.abs(got - exact) <= ulp), "a stored key is more than one bf16 ulp from the exact value"
+    assert np.all(np.abs(got - exact) <= ulp + 2.0 ** -17), "a stored key is off by more than one bf16 ulp"
     assert np.mean(got_bits == want_bits) > 0.999
 
 
