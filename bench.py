@@ -33,6 +33,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 from speculative_decoding_draft_rmsnorm_gb300 import workloads as W  # noqa: E402
+from speculative_decoding_draft_rmsnorm_gb300.sharding import max_over_ranks  # noqa: E402
 
 METRIC = "DFlash block-attn TFLOP/s and K/V HBM GB/s, % of GB300 roofline"
 FALLBACK_HBM_GBS = 6800.0
@@ -268,11 +269,7 @@ def run_gpu(args, b: W.Batch, rank: int, world: int) -> dict | None:
     step_ms = [e[0].elapsed_time(e[2]) for e in ev]
     attn_ms = [e[1].elapsed_time(e[2]) for e in ev]
     total_ms = sum(step_ms)
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([total_ms], dtype=torch.float64, device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(total_ms, device="cuda")
 
     # ---- end to end through the public API with host buffers (pinned), copies timed
     pinned = {k: torch.from_numpy(np.ascontiguousarray(v).view(np.int16) if v.dtype == np.uint16 else

@@ -79,6 +79,10 @@ int check_sizes(int num_reqs, int64_t total_q, int hq, int hkv, int dh, int64_t 
 
 }  // namespace
 
+namespace dflash {
+int report_error(int code, const char* msg) { return fail(code, "%s", msg); }
+}  // namespace dflash
+
 extern "C" {
 
 const char* dflash_last_error(void) { return g_msg; }
@@ -153,10 +157,10 @@ int dflash_block_attention_plan(int num_reqs, int64_t total_q, int hq, int hkv, 
                                                          max_block_len, window, causal, out_dtype == DFLASH_OUT_F32,
                                                          flags, sms);
   const bool any = num_reqs > 0 && total_q > 0;
-  plan[0] = any ? (w.may_split ? 3 : 2) : 0;
-  plan[1] = w.tiles_per_split;
-  plan[2] = w.units_max;
-  plan[3] = any ? std::max(1, std::min(sms, w.units_max)) : 0;
+  plan[0] = any ? (w.balanced ? 3 : 2) : 0;
+  plan[1] = static_cast<int64_t>(std::ceil(w.tiles_bound / w.grid));
+  plan[2] = w.groups_max;
+  plan[3] = any ? w.grid : 0;
   plan[4] = static_cast<int64_t>((w.total + 255) / 256);
   return ok();
 }
@@ -192,6 +196,8 @@ int dflash_block_attention(const dflash_bf16* q_raw, const dflash_bf16* k_blk, c
   const int precise = out_dtype == DFLASH_OUT_F32 ? 1 : 0;
   const dflash::WorkspacePlan w = dflash::plan_workspace(num_reqs, total_q, hq, hkv, dh, total_ctx, max_ctx_len,
                                                          max_block_len, window, causal, precise, flags, sms);
+  if (w.tiles_bound > 2.0e9)
+    return fail(DFLASH_ERR_UNSUPPORTED, "too many key tiles for one call (%.3g)", w.tiles_bound);
   if (workspace_bytes < w.total)
     return fail(DFLASH_ERR_WORKSPACE, "workspace has %zu bytes; %zu are needed", workspace_bytes, w.total);
   char* ws = static_cast<char*>(workspace);
@@ -212,12 +218,11 @@ int dflash_block_attention(const dflash_bf16* q_raw, const dflash_bf16* k_blk, c
   h.eps = eps;
   const float sc = scale > 0.0f ? scale : 1.0f / std::sqrt(static_cast<float>(dh));
   h.scale_log2 = sc * 1.4426950408889634f;
-  h.tiles_per_split = w.tiles_per_split;
-  h.max_splits = w.max_splits;
-  h.units_max = w.units_max;
+  h.groups_max = w.groups_max;
+  h.grid = w.grid;
   h.max_ctx_len = max_ctx_len;
   h.max_block_len = max_block_len;
-  h.may_split = w.may_split;
+  h.balanced = w.balanced;
   h.num_sms = sms;
   h.q = q_raw;
   h.k_blk = k_blk;
@@ -236,9 +241,9 @@ int dflash_block_attention(const dflash_bf16* q_raw, const dflash_bf16* k_blk, c
   h.q_lo = precise ? reinterpret_cast<uint16_t*>(ws + w.q_lo) : nullptr;
   h.k_hat = reinterpret_cast<uint16_t*>(ws + w.k_hat);
   h.k_lo = precise ? reinterpret_cast<uint16_t*>(ws + w.k_lo) : nullptr;
-  h.units = reinterpret_cast<dflash::Unit*>(ws + w.units);
-  h.part_o = w.may_split ? reinterpret_cast<float*>(ws + w.part_o) : nullptr;
-  h.part_ml = w.may_split ? reinterpret_cast<float*>(ws + w.part_ml) : nullptr;
+  h.groups = reinterpret_cast<dflash::Group*>(ws + w.groups);
+  h.part_o = w.balanced ? reinterpret_cast<float*>(ws + w.part_o) : nullptr;
+  h.part_ml = w.balanced ? reinterpret_cast<float*>(ws + w.part_ml) : nullptr;
   dflash::make_rope_turns(dh, static_cast<double>(rope_theta), &h.turns);
   char msg[256] = "";
   cudaError_t e = dflash::launch_attention(h, static_cast<cudaStream_t>(stream), msg, sizeof msg);

@@ -10,15 +10,19 @@
 // Three launches, chained with programmatic dependent launch:
 //   A  prologue: q^ = rope(rmsnorm(q)), k^blk = rope(rmsnorm(k_blk)) into the workspace
 //      (bf16; in precise mode also the bf16 remainders), and, in block 0, the table of
-//      work units: (request, kv head, query tile, range of key tiles).
-//   B  attention: persistent CTAs, one per SM, walk their units round-robin.
+//      groups (request, kv head, query tile) with their key-tile counts and prefix offsets.
+//   B  attention: persistent CTAs, one per SM. Balanced (stream-K) schedule: the groups'
+//      key tiles are laid end to end and CTA c takes tiles [c*T/G, (c+1)*T/G), so every
+//      CTA streams the same number of K/V tiles whatever the raggedness; a group that
+//      straddles CTAs is processed as segments whose partials are combined in C.
 //      Warp 0 streams Q / K / V tiles with TMA (128-byte swizzle); warp 1 issues
 //      tcgen05 MMAs: S = Q K^T into tensor memory (M = 64 query rows = G heads x block
 //      tokens, N = 128 keys), and O += P V (N = Dh) from P in shared memory; warps 2-5
 //      run the online softmax (f32, base 2, lazy rescale of O in TMEM when the running
-//      maximum grows by more than 2^8) and the epilogue. A unit covering all of a
-//      request's keys writes the normalised output; a split unit writes (O, m, l).
-//   C  combine: merges the split partials of a unit group:
+//      maximum grows by more than 2^8) and the epilogue. A segment covering a whole
+//      group writes the normalised output; a partial segment writes (O, m, l) to one of
+//      its CTA's two partial slots (first segment: 2c, last: 2c+1).
+//   C  combine: merges the partials of each group that straddles CTAs:
 //      o = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s.
 //
 // TMEM map (512 columns): S[0] at column 0, S[1] at 128, O at 256. An M = 64 MMA puts
@@ -41,15 +45,20 @@ namespace dflash {
 struct PrologueParams {
   NormRopeJob job;
   const int32_t *qsl, *csl, *clen;
-  Unit* units;
+  Group* groups;
   uint32_t* hdr;
   int64_t total_q, total_ctx;
   int num_reqs, hkv, g, tpq, causal, window;
-  int tiles_per_split, max_splits, units_max, max_ctx_len, max_block_len;
+  int groups_max, max_ctx_len, max_block_len;
+  int blk_tile;  // keys per block-key tile: 128, or 64 when hi and lo halves share a tile
 };
 
-__device__ void build_units(const PrologueParams& p) {
-  __shared__ int s_scan[256];
+// Validates the device metadata and writes one Group per (request, kv head, query tile)
+// with its key-tile count and the global index of its first tile (prefix over groups).
+// hdr[1] = number of groups, hdr[2] = total tiles.
+__device__ void build_groups(const PrologueParams& p) {
+  __shared__ int s_cnt[256];
+  __shared__ long long s_til[256];
   __shared__ int s_bad_global;
   const int tid = threadIdx.x;
   if (tid == 0) {
@@ -61,10 +70,11 @@ __device__ void build_units(const PrologueParams& p) {
   }
   __syncthreads();
   const bool bad_global = s_bad_global != 0;
-  int running = 0;
+  int run_g = 0;
+  long long run_t = 0;
   for (int base = 0; base < p.num_reqs; base += 256) {
     const int r = base + tid;
-    int cnt = 0, B = 0, C = 0, lo = 0, nct = 0, n = 0, QT = 0, S = 0, c0 = 0, q0 = 0;
+    int cnt = 0, B = 0, C = 0, lo = 0, nct = 0, n = 0, QT = 0, c0 = 0, q0 = 0;
     if (r < p.num_reqs && !bad_global) {
       q0 = p.qsl[r];
       const int q1 = p.qsl[r + 1];
@@ -81,66 +91,70 @@ __device__ void build_units(const PrologueParams& p) {
       if (B > 0) {
         lo = (p.causal && p.window > 0) ? max(0, C - p.window + 1) : 0;
         nct = (C - lo + kTileKeys - 1) / kTileKeys;
-        n = nct + (B + kTileKeys - 1) / kTileKeys;
+        n = nct + (B + p.blk_tile - 1) / p.blk_tile;
         QT = (B + p.tpq - 1) / p.tpq;
-        S = (n + p.tiles_per_split - 1) / p.tiles_per_split;
-        S = min(max(S, 1), min(p.max_splits, n));
-        cnt = p.hkv * QT * S;
+        cnt = p.hkv * QT;
       }
     }
-    // block-wide exclusive scan of cnt
-    s_scan[tid] = cnt;
+    // block-wide inclusive scans of the group and tile counts
+    s_cnt[tid] = cnt;
+    s_til[tid] = static_cast<long long>(cnt) * n;
     __syncthreads();
     for (int off = 1; off < 256; off <<= 1) {
-      const int v = tid >= off ? s_scan[tid - off] : 0;
+      const int vc = tid >= off ? s_cnt[tid - off] : 0;
+      const long long vt = tid >= off ? s_til[tid - off] : 0;
       __syncthreads();
-      s_scan[tid] += v;
+      s_cnt[tid] += vc;
+      s_til[tid] += vt;
       __syncthreads();
     }
-    const int offset = running + s_scan[tid] - cnt;
-    const int chunk_total = s_scan[255];
+    const int goff = run_g + s_cnt[tid] - cnt;
+    const long long toff = run_t + s_til[tid] - static_cast<long long>(cnt) * n;
+    const int chunk_g = s_cnt[255];
+    const long long chunk_t = s_til[255];
     __syncthreads();
-    if (cnt > 0) {
-      for (int kvh = 0; kvh < p.hkv; ++kvh)
-        for (int qt = 0; qt < QT; ++qt) {
-          const int first = offset + (kvh * QT + qt) * S;
-          for (int s = 0; s < S; ++s) {
-            const int u = first + s;
-            if (u >= p.units_max) {
-              atomicOr(&p.hdr[0], kErrMetadata);
-              continue;
-            }
-            Unit U;
-            U.r = r;
-            U.kvh = kvh;
-            U.qt = qt;
-            U.t0 = (s * n) / S;
-            U.t1 = ((s + 1) * n) / S;
-            U.split = s;
-            U.nsplit = S;
-            U.first = first;
-            U.clen = C;
-            U.blen = B;
-            U.ctx_lo = lo;
-            U.n_ctx_tiles = nct;
-            U.csl = c0;
-            U.qsl = q0;
-            U.tok0 = qt * p.tpq;
-            U.rows = min(p.tpq, B - U.tok0) * p.g;
-            p.units[u] = U;
-          }
-        }
+    for (int k = 0; k < cnt; ++k) {
+      const int gi = goff + k;
+      if (gi >= p.groups_max) {
+        atomicOr(&p.hdr[0], kErrMetadata);
+        break;
+      }
+      Group G;
+      G.r = r;
+      G.kvh = k / QT;
+      G.qt = k % QT;
+      G.n = n;
+      G.start = static_cast<int>(toff + static_cast<long long>(k) * n);
+      G.clen = C;
+      G.blen = B;
+      G.ctx_lo = lo;
+      G.n_ctx_tiles = nct;
+      G.csl = c0;
+      G.qsl = q0;
+      G.tok0 = G.qt * p.tpq;
+      G.rows = min(p.tpq, B - G.tok0) * p.g;
+      G.pad0 = G.pad1 = G.pad2 = 0;
+      p.groups[gi] = G;
     }
-    running += chunk_total;
+    run_g += chunk_g;
+    run_t += chunk_t;
   }
-  if (tid == 0) p.hdr[1] = static_cast<uint32_t>(min(running, p.units_max));
+  if (tid == 0) {
+    if (run_g > p.groups_max || run_t > 0x7fffffffLL) {  // cannot happen with valid host bounds
+      atomicOr(&p.hdr[0], kErrMetadata);
+      run_g = 0;
+      run_t = 0;
+    }
+    p.hdr[1] = static_cast<uint32_t>(run_g);
+    p.hdr[2] = static_cast<uint32_t>(run_t);
+  }
 }
 
 template <int DH>
 __global__ void __launch_bounds__(256) prologue_kernel(const __grid_constant__ PrologueParams p) {
   grid_dependents_launch();
   if (blockIdx.x == 0) {
-    build_units(p);
+    build_groups(p);
     return;
   }
   const int64_t warp_id = (static_cast<int64_t>(blockIdx.x - 1) * blockDim.x + threadIdx.x) >> 5;
@@ -149,15 +163,20 @@ __global__ void __launch_bounds__(256) prologue_kernel(const __grid_constant__ P
 }
 
 // ================================================================ kernel B
-template <int DH, int NK, int NV>
+// Shared-memory plan. NQ query buffers (hi, and lo in precise mode), two P buffers (hi,
+// and lo in precise mode), an NK-stage K ring and an NV-stage V ring; 1024-byte aligned
+// tiles (128-byte swizzle atoms).
+template <int DH, int NK, int NV, int NQ, bool PRECISE>
 struct Layout {
   static constexpr int NB = DH / 64;                  // 128-byte column blocks per row
-  static constexpr int QB = kTileRows * DH * 2;       // Q tile
-  static constexpr int PB = kTileRows * kTileKeys * 2;  // P tile
+  static constexpr int QB = kTileRows * DH * 2;       // Q tile (one part)
+  static constexpr int QBT = QB * (PRECISE ? 2 : 1);  // one Q buffer: hi [+ lo]
+  static constexpr int PB = kTileRows * kTileKeys * 2;  // P tile (one part)
+  static constexpr int PBT = PB * (PRECISE ? 2 : 1);  // one P buffer: hi [+ lo]
   static constexpr int KB = kTileKeys * DH * 2;       // K or V tile
   static constexpr int OFF_Q = 0;
-  static constexpr int OFF_P = OFF_Q + 2 * QB;
-  static constexpr int OFF_K = OFF_P + 2 * PB;
+  static constexpr int OFF_P = OFF_Q + NQ * QBT;
+  static constexpr int OFF_K = OFF_P + 2 * PBT;
   static constexpr int OFF_V = OFF_K + NK * KB;
   static constexpr int OFF_BAR = OFF_V + NV * KB;
   // barrier indices
@@ -167,17 +186,19 @@ struct Layout {
   static constexpr int DRAIN = Q_FULL + 14;  // final commit of the MMA thread (its own barrier)
   static constexpr int NBARS = Q_FULL + 15;
   static constexpr int OFF_MISC = OFF_BAR + NBARS * 8;
-  static constexpr int BYTES = OFF_MISC + 16;
+  static constexpr int BYTES = OFF_MISC + 64;
   static constexpr int ALLOC = BYTES + 1024;
 };
 
 struct AttnParams {
-  const Unit* units;
+  const Group* groups;
   uint32_t* hdr;
   float* part_o;
   float* part_ml;
   void* out;
-  int hq, g, out_f32, causal, window;
+  int hq, g, out_f32, causal, window, blk_tile;
+  int balanced;  // stream-K schedule (else one whole group per CTA, round-robin)
+  int grid;      // CTAs of the attention kernel (the combine kernel recomputes their ranges)
   float scale_log2;
 };
 
@@ -188,7 +209,7 @@ struct TileInfo {
   bool blk;   // block-key tile (else context tile)
 };
 
-__device__ __forceinline__ TileInfo tile_info(const Unit& U, int t) {
+__device__ __forceinline__ TileInfo tile_info(const Group& U, int t, int blk_tile) {
   TileInfo ti;
   if (t < U.n_ctx_tiles) {
     const int k0 = U.ctx_lo + t * kTileKeys;
@@ -197,28 +218,70 @@ __device__ __forceinline__ TileInfo tile_info(const Unit& U, int t) {
     ti.j0 = k0;
     ti.blk = false;
   } else {
-    const int k0 = (t - U.n_ctx_tiles) * kTileKeys;
+    const int k0 = (t - U.n_ctx_tiles) * blk_tile;
     ti.row = U.qsl + k0;
-    ti.valid = min(kTileKeys, U.blen - k0);
+    ti.valid = min(blk_tile, U.blen - k0);
     ti.j0 = U.clen + k0;
     ti.blk = true;
   }
   return ti;
 }
 
-__device__ __forceinline__ void load_unit(const Unit* units, int u, Unit& U) {
-  const int4* src = reinterpret_cast<const int4*>(units + u);
-  int4* dst = reinterpret_cast<int4*>(&U);
+__device__ __forceinline__ void load_group(const Group* groups, int g, Group& G) {
+  const int4* src = reinterpret_cast<const int4*>(groups + g);
+  int4* dst = reinterpret_cast<int4*>(&G);
 #pragma unroll
   for (int i = 0; i < 4; ++i) dst[i] = src[i];
 }
 
-template <int DH, int NK, int NV>
+// One segment of a CTA's work: key tiles [t0, t1) of one group.
+struct Seg {
+  Group grp;
+  int t0, t1;
+  int slot;       // partial slot (2 * cta + 0 for the CTA's first segment, + 1 otherwise)
+  bool complete;  // the segment covers the whole group
+};
+
+// Walks the segments of this CTA. Every role of the CTA runs its own copy and sees the
+// same sequence.
+struct SegIter {
+  const Group* groups;
+  long long lo, hi;  // balanced: this CTA's tile range
+  int ng, g, k;
+  bool balanced;
+  __device__ bool next(Seg& s) {
+    if (balanced) {
+      if (lo >= hi || g >= ng) return false;
+      load_group(groups, g, s.grp);
+      if (s.grp.start >= hi) return false;
+      const long long st = s.grp.start;
+      s.t0 = static_cast<int>((lo > st ? lo : st) - st);
+      const long long end = st + s.grp.n;
+      s.t1 = static_cast<int>((hi < end ? hi : end) - st);
+      s.complete = s.t0 == 0 && s.t1 == s.grp.n;
+      s.slot = 2 * static_cast<int>(blockIdx.x) + (k == 0 ? 0 : 1);
+      ++k;
+      ++g;
+      return true;
+    }
+    if (g >= ng) return false;
+    load_group(groups, g, s.grp);
+    s.t0 = 0;
+    s.t1 = s.grp.n;
+    s.complete = true;
+    s.slot = -1;
+    g += gridDim.x;
+    return true;
+  }
+};
+
+template <int DH, int NK, int NV, int NQ, bool PRECISE>
 __global__ void __launch_bounds__(192, 1)
 attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_kc,
                  const __grid_constant__ CUtensorMap tm_vc, const __grid_constant__ CUtensorMap tm_kb,
-                 const __grid_constant__ CUtensorMap tm_vb, const __grid_constant__ AttnParams p) {
-  using L = Layout<DH, NK, NV>;
+                 const __grid_constant__ CUtensorMap tm_vb, const __grid_constant__ CUtensorMap tm_ql,
+                 const __grid_constant__ CUtensorMap tm_kbl, const __grid_constant__ AttnParams p) {
+  using L = Layout<DH, NK, NV, NQ, PRECISE>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
@@ -261,6 +324,10 @@ attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     tma_prefetch_desc(&tm_vc);
     tma_prefetch_desc(&tm_kb);
     tma_prefetch_desc(&tm_vb);
+    if (PRECISE) {
+      tma_prefetch_desc(&tm_ql);
+      tma_prefetch_desc(&tm_kbl);
+    }
   }
   if (warp == 1) tmem_alloc(smem_u32(tmem_slot), 512);
   tc_fence_before();
@@ -268,9 +335,47 @@ attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  grid_dependency_wait();  // unit table and q^/k^ come from the prologue kernel
+  grid_dependency_wait();  // group table and q^/k^ come from the prologue kernel
   grid_dependents_launch();
-  const int n_units = static_cast<int>(p.hdr[1]);
+  long long* s_range = reinterpret_cast<long long*>(smem + L::OFF_MISC + 16);
+  int* s_first = reinterpret_cast<int*>(smem + L::OFF_MISC + 32);
+  if (tid == 0) {
+    const int ng = static_cast<int>(p.hdr[1]);
+    const long long tt = static_cast<long long>(p.hdr[2]);
+    long long lo = 0, hi = 0;
+    int g0 = blockIdx.x;
+    if (p.balanced) {
+      lo = static_cast<long long>(blockIdx.x) * tt / gridDim.x;
+      hi = static_cast<long long>(blockIdx.x + 1) * tt / gridDim.x;
+      int a = 0, b = ng - 1;  // last group whose first tile is <= lo
+      g0 = 0;
+      while (a <= b) {
+        const int m = (a + b) >> 1;
+        if (p.groups[m].start <= lo) {
+          g0 = m;
+          a = m + 1;
+        } else {
+          b = m - 1;
+        }
+      }
+    }
+    s_range[0] = lo;
+    s_range[1] = hi;
+    s_first[0] = g0;
+    s_first[1] = ng;
+  }
+  __syncthreads();
+  auto make_iter = [&]() {
+    SegIter it;
+    it.groups = p.groups;
+    it.lo = s_range[0];
+    it.hi = s_range[1];
+    it.g = s_first[0];
+    it.ng = s_first[1];
+    it.k = 0;
+    it.balanced = p.balanced != 0;
+    return it;
+  };
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
@@ -279,36 +384,46 @@ attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
       int iu = 0;
       bool ok = true;
       constexpr uint32_t q_box_bytes_per_row = 128;
-      for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++iu) {
-        Unit U;
-        load_unit(p.units, u, U);
-        const int qb = iu & 1;
-        if (!(ok = mbar_wait(bar(L::Q_EMPTY + qb), ((iu >> 1) & 1) ^ 1, abort_flag))) break;
+      SegIter it = make_iter();
+      Seg sg;
+      for (; ok && it.next(sg); ++iu) {
+        const Group& U = sg.grp;
+        const int qb = iu % NQ;
+        if (!(ok = mbar_wait(bar(L::Q_EMPTY + qb), ((iu / NQ) & 1) ^ 1, abort_flag))) break;
         // the Q box is G x (64 / G) rows whatever this unit's row count
         const uint32_t q_rows = static_cast<uint32_t>(p.g * (kTileRows / p.g));
-        mbar_arrive_expect_tx(bar(L::Q_FULL + qb), L::NB * q_rows * q_box_bytes_per_row);
+        mbar_arrive_expect_tx(bar(L::Q_FULL + qb), (PRECISE ? 2 : 1) * L::NB * q_rows * q_box_bytes_per_row);
 #pragma unroll
-        for (int nb = 0; nb < L::NB; ++nb)
-          tma_load_4d(sbase + L::OFF_Q + qb * L::QB + nb * (kTileRows * 128), &tm_q, bar(L::Q_FULL + qb), nb * 64, 0,
+        for (int nb = 0; nb < L::NB; ++nb) {
+          tma_load_4d(sbase + L::OFF_Q + qb * L::QBT + nb * (kTileRows * 128), &tm_q, bar(L::Q_FULL + qb), nb * 64, 0,
                       U.kvh, U.qsl + U.tok0);
-        const int n = U.t1 - U.t0;
+          if (PRECISE)
+            tma_load_4d(sbase + L::OFF_Q + qb * L::QBT + L::QB + nb * (kTileRows * 128), &tm_ql, bar(L::Q_FULL + qb),
+                        nb * 64, 0, U.kvh, U.qsl + U.tok0);
+        }
+        const int n = sg.t1 - sg.t0;
         auto issue_k = [&](int t) -> bool {
           const int slot = static_cast<int>(gk % NK);
           if (!mbar_wait(bar(L::K_EMPTY + slot), ((gk / NK) & 1) ^ 1, abort_flag)) return false;
-          const TileInfo ti = tile_info(U, t);
+          const TileInfo ti = tile_info(U, t, p.blk_tile);
           mbar_arrive_expect_tx(bar(L::K_FULL + slot), L::KB);
           const void* map = ti.blk ? static_cast<const void*>(&tm_kb) : static_cast<const void*>(&tm_kc);
 #pragma unroll
-          for (int nb = 0; nb < L::NB; ++nb)
+          for (int nb = 0; nb < L::NB; ++nb) {
             tma_load_3d(sbase + L::OFF_K + slot * L::KB + nb * (kTileKeys * 128), map, bar(L::K_FULL + slot), nb * 64,
                         U.kvh, ti.row);
+            // precise mode: a block tile holds 64 keys, hi in rows 0-63 and lo in rows 64-127
+            if (PRECISE && ti.blk)
+              tma_load_3d(sbase + L::OFF_K + slot * L::KB + nb * (kTileKeys * 128) + 64 * 128, &tm_kbl,
+                          bar(L::K_FULL + slot), nb * 64, U.kvh, ti.row);
+          }
           ++gk;
           return true;
         };
         auto issue_v = [&](int t) -> bool {
           const int slot = static_cast<int>(gv % NV);
           if (!mbar_wait(bar(L::V_EMPTY + slot), ((gv / NV) & 1) ^ 1, abort_flag)) return false;
-          const TileInfo ti = tile_info(U, t);
+          const TileInfo ti = tile_info(U, t, p.blk_tile);
           mbar_arrive_expect_tx(bar(L::V_FULL + slot), L::KB);
           const void* map = ti.blk ? static_cast<const void*>(&tm_vb) : static_cast<const void*>(&tm_vc);
 #pragma unroll
@@ -318,10 +433,10 @@ attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
           ++gv;
           return true;
         };
-        if (!(ok = issue_k(U.t0))) break;
+        if (!(ok = issue_k(sg.t0))) break;
         for (int j = 0; j < n && ok; ++j) {
-          if (j + 1 < n) ok = issue_k(U.t0 + j + 1);
-          if (ok) ok = issue_v(U.t0 + j);
+          if (j + 1 < n) ok = issue_k(sg.t0 + j + 1);
+          if (ok) ok = issue_v(sg.t0 + j);
         }
       }
       if (!ok) atomicOr(&p.hdr[0], kErrTimeout);
@@ -347,14 +462,15 @@ attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
       int iu = 0;
       bool ok = true;
       const uint32_t idesc_pv = umma_idesc_bf16(kTileRows, DH, 0, 1);
-      for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++iu) {
-        Unit U;
-        load_unit(p.units, u, U);
-        const int qb = iu & 1;
-        const int n = U.t1 - U.t0;
-        if (!(ok = mbar_wait(bar(L::Q_FULL + qb), (iu >> 1) & 1, abort_flag))) break;
+      SegIter it = make_iter();
+      Seg sg;
+      for (; ok && it.next(sg); ++iu) {
+        const Group& U = sg.grp;
+        const int qb = iu % NQ;
+        const int n = sg.t1 - sg.t0;
+        if (!(ok = mbar_wait(bar(L::Q_FULL + qb), (iu / NQ) & 1, abort_flag))) break;
         tc_fence_after();
-        const uint32_t q_addr = sbase + L::OFF_Q + qb * L::QB;
+        const uint32_t q_addr = sbase + L::OFF_Q + qb * L::QBT;
         auto issue_qk = [&](int j) -> bool {
           const uint32_t g = gj + j;
           const int sb = g & 1;
@@ -362,15 +478,23 @@ attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
           if (!mbar_wait(bar(L::K_FULL + slot), (gk / NK) & 1, abort_flag)) return false;
           if (!mbar_wait(bar(L::S_EMPTY + sb), ((g >> 1) & 1) ^ 1, abort_flag)) return false;
           tc_fence_after();
-          const TileInfo ti = tile_info(U, U.t0 + j);
+          const TileInfo ti = tile_info(U, sg.t0 + j, p.blk_tile);
           const int nq = min(kTileKeys, (ti.valid + 15) & ~15);
           const uint32_t idesc = umma_idesc_bf16(kTileRows, nq, 0, 0);
           const uint32_t k_addr = sbase + L::OFF_K + slot * L::KB;
 #pragma unroll
           for (int kk = 0; kk < DH / 16; ++kk) {
-            const uint64_t a = umma_desc_sw128(q_addr + (kk >> 2) * (kTileRows * 128) + (kk & 3) * 32, 16, 1024);
-            const uint64_t b = umma_desc_sw128(k_addr + (kk >> 2) * (kTileKeys * 128) + (kk & 3) * 32, 16, 1024);
-            umma_bf16_ss(tmem + sb * 128, a, b, idesc, kk > 0 ? 1u : 0u);
+            const uint32_t qo = (kk >> 2) * (kTileRows * 128) + (kk & 3) * 32;
+            const uint32_t ko = (kk >> 2) * (kTileKeys * 128) + (kk & 3) * 32;
+            const uint64_t b = umma_desc_sw128(k_addr + ko, 16, 1024);
+            umma_bf16_ss(tmem + sb * 128, umma_desc_sw128(q_addr + qo, 16, 1024), b, idesc, kk > 0 ? 1u : 0u);
+            if (PRECISE) {
+              // S = Q_hi K + Q_lo K (+ Q_hi K_lo on block tiles, whose keys are rounded here)
+              umma_bf16_ss(tmem + sb * 128, umma_desc_sw128(q_addr + L::QB + qo, 16, 1024), b, idesc, 1u);
+              if (ti.blk)
+                umma_bf16_ss(tmem + sb * 128, umma_desc_sw128(q_addr + qo, 16, 1024),
+                             umma_desc_sw128(k_addr + ko + 64 * 128, 16, 1024), idesc, 1u);
+            }
           }
           umma_commit(bar(L::S_FULL + sb));
           umma_commit(bar(L::K_EMPTY + slot));
@@ -388,14 +512,15 @@ attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
           if (!(ok = mbar_wait(bar(L::V_FULL + vslot), (gv / NV) & 1, abort_flag))) break;
           if (j == 0 && !(ok = mbar_wait(bar(L::O_EMPTY), (iu & 1) ^ 1, abort_flag))) break;
           tc_fence_after();
-          const TileInfo ti = tile_info(U, U.t0 + j);
+          const TileInfo ti = tile_info(U, sg.t0 + j, p.blk_tile);
           const int ksteps = (ti.valid + 15) >> 4;
-          const uint32_t p_addr = sbase + L::OFF_P + pb * L::PB;
+          const uint32_t p_addr = sbase + L::OFF_P + pb * L::PBT;
           const uint32_t v_addr = sbase + L::OFF_V + vslot * L::KB;
           for (int kk = 0; kk < ksteps; ++kk) {
-            const uint64_t a = umma_desc_sw128(p_addr + (kk >> 2) * (kTileRows * 128) + (kk & 3) * 32, 16, 1024);
+            const uint32_t po = (kk >> 2) * (kTileRows * 128) + (kk & 3) * 32;
             const uint64_t b = umma_desc_sw128(v_addr + kk * (16 * 128), kTileKeys * 128, 1024);
-            umma_bf16_ss(tmem + 256, a, b, idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
+            umma_bf16_ss(tmem + 256, umma_desc_sw128(p_addr + po, 16, 1024), b, idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
+            if (PRECISE) umma_bf16_ss(tmem + 256, umma_desc_sw128(p_addr + L::PB + po, 16, 1024), b, idesc_pv, 1u);
           }
           umma_commit(bar(L::V_EMPTY + vslot));
           umma_commit(bar(L::P_EMPTY + pb));
@@ -426,10 +551,11 @@ attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
       if (lane == 0) r = mbar_wait(b, parity, abort_flag) ? 1 : 0;
       return __shfl_sync(0xffffffffu, r, 0) != 0;
     };
-    for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++iu) {
-      Unit U;
-      load_unit(p.units, u, U);
-      const int n = U.t1 - U.t0;
+    SegIter it = make_iter();
+    Seg sg;
+    for (; ok && it.next(sg); ++iu) {
+      const Group& U = sg.grp;
+      const int n = sg.t1 - sg.t0;
       const bool row_ok = rho < U.rows;
       const int b = U.tok0 + rho / p.g;        // block index of this row
       const int i = U.clen + b;                // combined query index
@@ -446,7 +572,7 @@ attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
       for (int j = 0; j < n; ++j) {
         const uint32_t g = gj + j;
         const int sb = g & 1;
-        const TileInfo ti = tile_info(U, U.t0 + j);
+        const TileInfo ti = tile_info(U, sg.t0 + j, p.blk_tile);
         if (!(ok = wait_warp(bar(L::S_FULL + sb), (g >> 1) & 1))) break;
         tc_fence_after();
         uint32_t sr[64];
@@ -512,6 +638,7 @@ attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         }
         const float m_eff = m_used == -INFINITY ? 0.0f : m_used;
         uint32_t pk[32];
+        uint32_t pl[PRECISE ? 32 : 1];
         float lsum = 0.0f;
 #pragma unroll
         for (int c = 0; c < 64; c += 2) {
@@ -519,17 +646,27 @@ attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
           const float p1 = ex2_approx(x[c + 1] - m_eff);
           const uint32_t v = pack_bf16x2(p0, p1);
           pk[c / 2] = v;
-          lsum += bf16lo_to_f32(v) + bf16hi_to_f32(v);
+          if (PRECISE) {
+            // P = P_hi + P_lo; l sums the unrounded weights
+            pl[c / 2] = pack_bf16x2(p0 - bf16lo_to_f32(v), p1 - bf16hi_to_f32(v));
+            lsum += p0 + p1;
+          } else {
+            lsum += bf16lo_to_f32(v) + bf16hi_to_f32(v);  // l sums exactly the weights PV uses
+          }
         }
         l += lsum;
         // the P buffer is free once PV of tile g-2 has completed
         if (!(ok = wait_warp(bar(L::P_EMPTY + sb), ((g >> 1) & 1) ^ 1))) break;
         {
-          uint8_t* prow = smem + L::OFF_P + sb * L::PB + half * (kTileRows * 128) + rho * 128;
+          uint8_t* prow = smem + L::OFF_P + sb * L::PBT + half * (kTileRows * 128) + rho * 128;
 #pragma unroll
           for (int chn = 0; chn < 8; ++chn) {
             uint4 v = make_uint4(pk[4 * chn], pk[4 * chn + 1], pk[4 * chn + 2], pk[4 * chn + 3]);
             *reinterpret_cast<uint4*>(prow + ((chn ^ (rho & 7)) << 4)) = v;
+            if (PRECISE) {
+              uint4 w = make_uint4(pl[4 * chn], pl[4 * chn + 1], pl[4 * chn + 2], pl[4 * chn + 3]);
+              *reinterpret_cast<uint4*>(prow + L::PB + ((chn ^ (rho & 7)) << 4)) = w;
+            }
           }
         }
         if (ti.valid & 15) {
@@ -571,7 +708,7 @@ attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         const int gi = rho % p.g;
         const int64_t tok = U.qsl + b;
         const int head = U.kvh * p.g + gi;
-        if (U.nsplit == 1) {
+        if (sg.complete) {
           const float inv = l_tot > 0.0f ? 1.0f / l_tot : 0.0f;
           if (p.out_f32) {
             float* dst = reinterpret_cast<float*>(p.out) + (tok * p.hq + head) * DH + half * (DH / 2);
@@ -597,7 +734,7 @@ attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
               }
           }
         } else {
-          float* dst = p.part_o + (static_cast<int64_t>(u) * kTileRows + rho) * DH + half * (DH / 2);
+          float* dst = p.part_o + (static_cast<int64_t>(sg.slot) * kTileRows + rho) * DH + half * (DH / 2);
 #pragma unroll
           for (int ch = 0; ch < CH; ++ch)
 #pragma unroll
@@ -606,7 +743,7 @@ attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                   make_float4(__uint_as_float(o[ch][e]), __uint_as_float(o[ch][e + 1]), __uint_as_float(o[ch][e + 2]),
                               __uint_as_float(o[ch][e + 3]));
           if (half == 0) {
-            float* ml = p.part_ml + (static_cast<int64_t>(u) * kTileRows + rho) * 2;
+            float* ml = p.part_ml + (static_cast<int64_t>(sg.slot) * kTileRows + rho) * 2;
             ml[0] = m_used;
             ml[1] = l_tot;
           }
@@ -628,37 +765,43 @@ attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
 template <int DH>
 __global__ void __launch_bounds__(256) combine_kernel(const __grid_constant__ AttnParams p) {
   grid_dependency_wait();
-  const int u = blockIdx.x;
-  const int n_units = static_cast<int>(p.hdr[1]);
-  if (u >= n_units) return;
-  Unit U;
-  load_unit(p.units, u, U);
-  if (U.split != 0 || U.nsplit <= 1) return;
-  if (u + U.nsplit > n_units) {  // group cut short by a truncated unit table
-    if (threadIdx.x == 0) atomicOr(&p.hdr[0], kErrMetadata);
-    return;
-  }
+  const int gi = blockIdx.x;
+  const int ng = static_cast<int>(p.hdr[1]);
+  const long long tt = static_cast<long long>(p.hdr[2]);
+  if (gi >= ng || !p.balanced || tt <= 0) return;
+  Group G;
+  load_group(p.groups, gi, G);
+  const long long grid = p.grid;
+  // CTA c of the attention kernel owned tiles [c*tt/grid, (c+1)*tt/grid)
+  auto cta_of = [&](long long t) { return ((t + 1) * grid + tt - 1) / tt - 1; };
+  const long long ca = cta_of(G.start), cb = cta_of(static_cast<long long>(G.start) + G.n - 1);
+  if (ca == cb) return;  // the group was finished by one CTA
+  const bool ca_first = ca * tt / grid >= G.start;  // the group is CTA ca's first segment
   constexpr int CPR = DH / 8;  // 8-float chunks per row
-  for (int item = threadIdx.x; item < U.rows * CPR; item += blockDim.x) {
+  for (int item = threadIdx.x; item < G.rows * CPR; item += blockDim.x) {
     const int rho = item / CPR;
     const int c8 = (item % CPR) * 8;
     float M = -INFINITY;
-    for (int s = 0; s < U.nsplit; ++s) M = fmaxf(M, p.part_ml[(static_cast<int64_t>(u + s) * kTileRows + rho) * 2]);
+    for (long long c = ca; c <= cb; ++c) {
+      const long long slot = 2 * c + ((c == ca && !ca_first) ? 1 : 0);
+      M = fmaxf(M, p.part_ml[(slot * kTileRows + rho) * 2]);
+    }
     const float Me = M == -INFINITY ? 0.0f : M;
     float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
     float L = 0.0f;
-    for (int s = 0; s < U.nsplit; ++s) {
-      const float* ml = p.part_ml + (static_cast<int64_t>(u + s) * kTileRows + rho) * 2;
+    for (long long c = ca; c <= cb; ++c) {
+      const long long slot = 2 * c + ((c == ca && !ca_first) ? 1 : 0);
+      const float* ml = p.part_ml + (slot * kTileRows + rho) * 2;
       const float w = ml[0] == -INFINITY ? 0.0f : ex2_approx(ml[0] - Me);
       L += w * ml[1];
-      const float4* src = reinterpret_cast<const float4*>(p.part_o + (static_cast<int64_t>(u + s) * kTileRows + rho) * DH + c8);
+      const float4* src = reinterpret_cast<const float4*>(p.part_o + (slot * kTileRows + rho) * DH + c8);
       const float4 a = src[0], b = src[1];
       acc[0] += w * a.x; acc[1] += w * a.y; acc[2] += w * a.z; acc[3] += w * a.w;
       acc[4] += w * b.x; acc[5] += w * b.y; acc[6] += w * b.z; acc[7] += w * b.w;
     }
     const float inv = L > 0.0f ? 1.0f / L : 0.0f;
-    const int64_t tok = U.qsl + U.tok0 + rho / p.g;
-    const int head = U.kvh * p.g + rho % p.g;
+    const int64_t tok = G.qsl + G.tok0 + rho / p.g;
+    const int head = G.kvh * p.g + rho % p.g;
     if (p.out_f32) {
       float* dst = reinterpret_cast<float*>(p.out) + (tok * p.hq + head) * DH + c8;
       *reinterpret_cast<float4*>(dst) = make_float4(acc[0] * inv, acc[1] * inv, acc[2] * inv, acc[3] * inv);
@@ -734,29 +877,29 @@ WorkspacePlan plan_workspace(int num_reqs, int64_t total_q, int hq, int hkv, int
   w.tpq = kTileRows / g;
   w.qt_max = max_block_len > 0 ? (max_block_len + w.tpq - 1) / w.tpq : 0;
   int ctx_tiles_max = (max_ctx_len + kTileKeys - 1) / kTileKeys;
-  if (causal && window > 0) ctx_tiles_max = std::min(ctx_tiles_max, (window - 1 + kTileKeys - 1) / kTileKeys);
-  const int blk_tiles_max = (max_block_len + kTileKeys - 1) / kTileKeys;
+  if (causal && window > 0) ctx_tiles_max = std::min(ctx_tiles_max, (window - 1 + kTileKeys - 1) / kTileKeys + 1);
+  const int blk_tile = precise ? 64 : kTileKeys;
+  const int blk_tiles_max = (max_block_len + blk_tile - 1) / blk_tile;
   const int n_max = std::max(1, ctx_tiles_max + blk_tiles_max);
-  // tiles over all requests (per kv head and query tile), an upper bound from capacities
-  double tiles_bound = static_cast<double>(total_ctx) / kTileKeys + static_cast<double>(num_reqs) * (1 + blk_tiles_max);
-  if (causal && window > 0)
-    tiles_bound = std::min(tiles_bound, static_cast<double>(num_reqs) * n_max);
-  // aim for about two units per SM (tunable with DFLASH_TILES_PER_SPLIT)
-  const double est = static_cast<double>(hkv) * std::max(1, w.qt_max) * tiles_bound;
-  int tps = static_cast<int>(std::ceil(est / std::max(1, 2 * num_sms)));
-  tps = std::max(tps, 4);
-  if (const char* e = std::getenv("DFLASH_TILES_PER_SPLIT")) {
-    const int v = std::atoi(e);
-    if (v > 0) tps = v;
+  // key tiles of all groups: an upper bound from the segment capacities and the lengths
+  double per_head = static_cast<double>(total_ctx) / kTileKeys + static_cast<double>(num_reqs) * (1 + blk_tiles_max);
+  per_head = std::min(per_head, static_cast<double>(num_reqs) * n_max);
+  w.tiles_bound = static_cast<double>(hkv) * std::max(1, w.qt_max) * per_head;
+  w.groups_max = std::max(1, num_reqs * hkv * std::max(1, w.qt_max));
+  w.balanced = (flags & 2) == 0;  // DFLASH_FLAG_NO_SPLIT selects whole groups per CTA
+  if (w.balanced) {
+    // every CTA should stream at least kMinTilesPerCta tiles so that its set-up is amortised
+    constexpr double kMinTilesPerCta = 8.0;
+    w.grid = static_cast<int>(std::min<double>(num_sms, std::max(1.0, std::ceil(w.tiles_bound / kMinTilesPerCta))));
+  } else {
+    w.grid = std::min(num_sms, w.groups_max);
   }
-  if (flags & 2) tps = n_max;                                   // DFLASH_FLAG_NO_SPLIT
-  if (flags & 1) tps = std::min(tps, std::max(1, (n_max + 1) / 2));  // DFLASH_FLAG_FORCE_SPLIT
-  w.tiles_per_split = tps;
-  w.max_splits = std::max(1, (n_max + tps - 1) / tps);
-  w.may_split = w.max_splits > 1;
-  const double sum_splits = std::min(tiles_bound / tps + num_reqs, static_cast<double>(num_reqs) * w.max_splits);
-  const double units = static_cast<double>(hkv) * std::max(1, w.qt_max) * sum_splits;
-  w.units_max = static_cast<int>(std::min(units + 1.0, 2.0e9 / 64.0));
+  if (const char* e = std::getenv("DFLASH_GRID")) {  // tuning sweeps
+    const int v = std::atoi(e);
+    if (v > 0) w.grid = std::min(v, num_sms);
+  }
+  w.grid = std::max(1, w.grid);
+  w.parts = w.balanced ? 2 * w.grid : 0;
   size_t off = 0;
   w.hdr = off;
   off += 256;
@@ -768,23 +911,23 @@ WorkspacePlan plan_workspace(int num_reqs, int64_t total_q, int hq, int hkv, int
   off += align256(static_cast<size_t>(total_q) * hkv * dh * 2);
   w.k_lo = off;
   if (precise) off += align256(static_cast<size_t>(total_q) * hkv * dh * 2);
-  w.units = off;
-  off += align256(static_cast<size_t>(w.units_max) * sizeof(Unit));
+  w.groups = off;
+  off += align256(static_cast<size_t>(w.groups_max) * sizeof(Group));
   w.part_o = off;
-  if (w.may_split) off += align256(static_cast<size_t>(w.units_max) * kTileRows * dh * 4);
+  off += align256(static_cast<size_t>(w.parts) * kTileRows * dh * 4);
   w.part_ml = off;
-  if (w.may_split) off += align256(static_cast<size_t>(w.units_max) * kTileRows * 2 * 4);
+  off += align256(static_cast<size_t>(w.parts) * kTileRows * 2 * 4);
   w.total = off;
   return w;
 }
 
-template <int DH, int NK, int NV>
+template <int DH, int NK, int NV, int NQ, bool PRECISE>
 static cudaError_t launch_b(const CUtensorMap& tq, const CUtensorMap& tkc, const CUtensorMap& tvc,
-                            const CUtensorMap& tkb, const CUtensorMap& tvb, const AttnParams& ap, int grid,
-                            cudaStream_t stream) {
-  using L = Layout<DH, NK, NV>;
+                            const CUtensorMap& tkb, const CUtensorMap& tvb, const CUtensorMap& tql,
+                            const CUtensorMap& tkbl, const AttnParams& ap, int grid, cudaStream_t stream) {
+  using L = Layout<DH, NK, NV, NQ, PRECISE>;
   static_assert(L::ALLOC <= 232448, "shared memory plan exceeds the per-block limit");
-  auto kern = attention_kernel<DH, NK, NV>;
+  auto kern = attention_kernel<DH, NK, NV, NQ, PRECISE>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg{};
@@ -797,7 +940,7 @@ static cudaError_t launch_b(const CUtensorMap& tq, const CUtensorMap& tkc, const
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, tq, tkc, tvc, tkb, tvb, ap);
+  return cudaLaunchKernelEx(&cfg, kern, tq, tkc, tvc, tkb, tvb, tql, tkbl, ap);
 }
 
 template <int DH>
@@ -832,7 +975,7 @@ cudaError_t launch_attention(const AttnHost& h, cudaStream_t stream, char* msg, 
   pp.qsl = h.qsl;
   pp.csl = h.csl;
   pp.clen = h.clen;
-  pp.units = h.units;
+  pp.groups = h.groups;
   pp.hdr = h.ws_hdr;
   pp.total_q = h.total_q;
   pp.total_ctx = h.total_ctx;
@@ -842,11 +985,10 @@ cudaError_t launch_attention(const AttnHost& h, cudaStream_t stream, char* msg, 
   pp.tpq = h.tpq;
   pp.causal = h.causal;
   pp.window = h.window;
-  pp.tiles_per_split = h.tiles_per_split;
-  pp.max_splits = h.max_splits;
-  pp.units_max = h.units_max;
+  pp.groups_max = h.groups_max;
   pp.max_ctx_len = h.max_ctx_len;
   pp.max_block_len = h.max_block_len;
+  pp.blk_tile = h.precise ? 64 : kTileKeys;
   cudaError_t e = cudaSuccess;
   int64_t nr_blocks = (h.total_q + 7) / 8;
   nr_blocks = std::min<int64_t>(nr_blocks, static_cast<int64_t>(h.num_sms) * 2);  // all co-resident
@@ -858,21 +1000,28 @@ cudaError_t launch_attention(const AttnHost& h, cudaStream_t stream, char* msg, 
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
   // ---- tensor maps
-  CUtensorMap tq, tkc, tvc, tkb, tvb;
+  CUtensorMap tq, tkc, tvc, tkb, tvb, tql, tkbl;
   const void* ctx_k = h.total_ctx > 0 ? static_cast<const void*>(h.ctx_k) : static_cast<const void*>(h.q_hat);
   const void* ctx_v = h.total_ctx > 0 ? static_cast<const void*>(h.ctx_v) : static_cast<const void*>(h.q_hat);
   const int64_t ctx_rows = h.total_ctx > 0 ? h.total_ctx : 1;
   bool ok = encode_q_map(&tq, h.q_hat, h.dh, h.g, h.hkv, h.total_q, h.tpq) &&
             encode_rows_map(&tkc, ctx_k, h.dh, h.hkv, ctx_rows, kTileKeys) &&
             encode_rows_map(&tvc, ctx_v, h.dh, h.hkv, ctx_rows, kTileKeys) &&
-            encode_rows_map(&tkb, h.k_hat, h.dh, h.hkv, h.total_q, kTileKeys) &&
+            encode_rows_map(&tkb, h.k_hat, h.dh, h.hkv, h.total_q, h.precise ? 64 : kTileKeys) &&
             encode_rows_map(&tvb, h.v_blk, h.dh, h.hkv, h.total_q, kTileKeys);
+  if (ok && h.precise)
+    ok = encode_q_map(&tql, h.q_lo, h.dh, h.g, h.hkv, h.total_q, h.tpq) &&
+         encode_rows_map(&tkbl, h.k_lo, h.dh, h.hkv, h.total_q, 64);
+  if (!h.precise) {
+    tql = tq;
+    tkbl = tkb;
+  }
   if (!ok) {
     std::snprintf(msg, msg_len, "cuTensorMapEncodeTiled failed (driver entry point or tensor layout)");
     return cudaErrorInvalidValue;
   }
   AttnParams ap{};
-  ap.units = h.units;
+  ap.groups = h.groups;
   ap.hdr = h.ws_hdr;
   ap.part_o = h.part_o;
   ap.part_ml = h.part_ml;
@@ -883,19 +1032,24 @@ cudaError_t launch_attention(const AttnHost& h, cudaStream_t stream, char* msg, 
   ap.causal = h.causal;
   ap.window = h.window;
   ap.scale_log2 = h.scale_log2;
-  const int grid_b = std::max(1, std::min(h.num_sms, h.units_max));
+  ap.blk_tile = h.precise ? 64 : kTileKeys;
+  ap.balanced = h.balanced ? 1 : 0;
+  ap.grid = h.grid;
+  const int grid_b = h.grid;
   // ---- B: attention
   if (h.dh == 128)
-    e = launch_b<128, 3, 2>(tq, tkc, tvc, tkb, tvb, ap, grid_b, stream);
+    e = h.precise ? launch_b<128, 2, 2, 1, true>(tq, tkc, tvc, tkb, tvb, tql, tkbl, ap, grid_b, stream)
+                  : launch_b<128, 3, 2, 2, false>(tq, tkc, tvc, tkb, tvb, tql, tkbl, ap, grid_b, stream);
   else
-    e = launch_b<64, 4, 4>(tq, tkc, tvc, tkb, tvb, ap, grid_b, stream);
+    e = h.precise ? launch_b<64, 3, 3, 2, true>(tq, tkc, tvc, tkb, tvb, tql, tkbl, ap, grid_b, stream)
+                  : launch_b<64, 4, 4, 2, false>(tq, tkc, tvc, tkb, tvb, tql, tkbl, ap, grid_b, stream);
   if (e != cudaSuccess) return e;
   // ---- C: combine split partials
-  if (h.may_split) {
+  if (h.balanced) {
     if (h.dh == 128)
-      e = launch_c<128>(ap, h.units_max, stream);
+      e = launch_c<128>(ap, h.groups_max, stream);
     else
-      e = launch_c<64>(ap, h.units_max, stream);
+      e = launch_c<64>(ap, h.groups_max, stream);
   }
   return e;
 }

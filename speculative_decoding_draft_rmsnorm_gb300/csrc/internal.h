@@ -50,16 +50,15 @@ struct NormRopeJob {
 
 cudaError_t launch_norm_rope(const NormRopeJob& job, int dh, int num_sms, cudaStream_t stream);
 
-// Work unit of the attention kernel: one (request, kv head, query tile) and a
-// contiguous range [t0, t1) of that request's key tiles (context tiles first, then
-// block tiles).
-struct Unit {
-  int r, kvh, qt, t0;
-  int t1, split, nsplit, first;     // first = unit index of split 0 of this group
-  int clen, blen, ctx_lo, n_ctx_tiles;
-  int csl, qsl, rows, tok0;         // rows of this q tile; tok0 = first block index
+// One group of the attention kernel's work: (request, kv head, query tile) with its n key
+// tiles (context tiles first, then block tiles) at global tile indices [start, start+n).
+struct Group {
+  int r, kvh, qt, n;
+  int start, clen, blen, ctx_lo;
+  int n_ctx_tiles, csl, qsl, rows;  // rows of this query tile (G heads x tokens)
+  int tok0, pad0, pad1, pad2;       // tok0 = first block index of the query tile
 };
-static_assert(sizeof(Unit) == 64, "unit descriptor is 64 bytes");
+static_assert(sizeof(Group) == 64, "group descriptor is 64 bytes");
 
 struct AttnHost {
   // sizes
@@ -67,27 +66,28 @@ struct AttnHost {
   int64_t total_q, total_ctx;
   int causal, window, out_f32, precise;
   float eps, scale_log2;
-  int tiles_per_split, max_splits, units_max;
+  int groups_max, grid;
   int max_ctx_len, max_block_len;
-  bool may_split;
+  bool balanced;
   int num_sms;
   // device pointers
   const uint16_t *q, *k_blk, *v_blk, *ctx_k, *ctx_v, *q_norm_w, *k_norm_w;
   const int32_t *qsl, *csl, *clen, *positions;
   void* out;
   // workspace carve-up
-  uint32_t* ws_hdr;   // [0] error word, [1] unit count
+  uint32_t* ws_hdr;   // [0] error word, [1] group count, [2] total key tiles
   uint16_t *q_hat, *q_lo, *k_hat, *k_lo;
-  Unit* units;
-  float* part_o;      // [units_max][64][dh]
-  float* part_ml;     // [units_max][64][2]
+  Group* groups;
+  float* part_o;      // [2 * grid][64][dh]  partial O of straddling segments
+  float* part_ml;     // [2 * grid][64][2]   their running max (log2 units) and weight sum
   RopeTurns turns;
 };
 
 struct WorkspacePlan {
-  size_t hdr, q_hat, q_lo, k_hat, k_lo, units, part_o, part_ml, total;
-  int tiles_per_split, max_splits, units_max, qt_max, tpq;
-  bool may_split;
+  size_t hdr, q_hat, q_lo, k_hat, k_lo, groups, part_o, part_ml, total;
+  int groups_max, grid, parts, qt_max, tpq;
+  double tiles_bound;
+  bool balanced;
 };
 
 WorkspacePlan plan_workspace(int num_reqs, int64_t total_q, int hq, int hkv, int dh, int64_t total_ctx,
@@ -95,5 +95,8 @@ WorkspacePlan plan_workspace(int num_reqs, int64_t total_q, int hq, int hkv, int
                              int num_sms);
 
 cudaError_t launch_attention(const AttnHost& h, cudaStream_t stream, char* msg, size_t msg_len);
+
+// Records `msg` as the thread's last error (what dflash_last_error returns) and returns code.
+int report_error(int code, const char* msg);
 
 }  // namespace dflash

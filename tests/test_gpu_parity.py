@@ -119,6 +119,31 @@ def test_block_attention_small_bf16(case):
     U.assert_close_bf16(got, want, name)
 
 
+F32_CASES = [c for c in SMALL_CASES if c[0] in ("tiny_cfg", "gqa4_dh128", "no_context", "ragged_blocks", "causal",
+                                               "swa", "swa_w1", "two_qtiles", "g8_qtiles")]
+
+
+@pytest.mark.parametrize("case", F32_CASES, ids=[c[0] for c in F32_CASES])
+def test_block_attention_small_f32(case):
+    # f32 output runs on split hi+lo bf16 operands (q^, block k^ and P), so it must sit
+    # within 2e-4 of the exact result even where few keys make every weight count
+    name, hq, hkv, dh, causal, window, cl, bl = case
+    b = W.make_batch(cfg(hq, hkv, dh, causal, window, seed=17), ctx_lens=cl, block_lens=bl)
+    ck = U.stored_ctx_k(b)
+    want = U.oracle_attention(b, ck)
+    got = U.dev_to_f64(U.gpu_attention(b, ck, out_dtype=1))
+    U.assert_close_f32(got, want, name)
+
+
+@pytest.mark.parametrize("flags", [1, 2])
+def test_f32_split_and_unsplit(flags):
+    b = W.make_batch(cfg(32, 8, 128, seed=18), ctx_lens=[1500, 0, 2000], block_lens=[16, 16, 16])
+    ck = U.stored_ctx_k(b)
+    want = U.oracle_attention(b, ck)
+    got = U.dev_to_f64(U.gpu_attention(b, ck, out_dtype=1, flags=flags))
+    U.assert_close_f32(got, want, f"f32 flags={flags}")
+
+
 @pytest.mark.parametrize("flags", [1, 2])
 def test_split_and_unsplit_paths_both_match(flags):
     b = W.make_batch(cfg(32, 8, 128, seed=8), ctx_lens=[1500, 700, 2000], block_lens=[16, 16, 16])
