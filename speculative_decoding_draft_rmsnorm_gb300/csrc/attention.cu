@@ -777,9 +777,10 @@ __global__ void __launch_bounds__(256) combine_kernel(const __grid_constant__ At
   const long long ca = cta_of(G.start), cb = cta_of(static_cast<long long>(G.start) + G.n - 1);
   if (ca == cb) return;  // the group was finished by one CTA
   const bool ca_first = ca * tt / grid >= G.start;  // the group is CTA ca's first segment
-  constexpr int CPR = DH / 8;  // 8-float chunks per row
-  for (int item = threadIdx.x; item < G.rows * CPR; item += blockDim.x) {
-    const int rho = item / CPR;
+  constexpr int CPR = DH / 8;  // 8-float chunks per row; block y covers rows [16y, 16y+16)
+  for (int item = threadIdx.x; item < 16 * CPR; item += blockDim.x) {
+    const int rho = 16 * static_cast<int>(blockIdx.y) + item / CPR;
+    if (rho >= G.rows) break;
     const int c8 = (item % CPR) * 8;
     float M = -INFINITY;
     for (long long c = ca; c <= cb; ++c) {
@@ -946,8 +947,8 @@ static cudaError_t launch_b(const CUtensorMap& tq, const CUtensorMap& tkc, const
 template <int DH>
 static cudaError_t launch_c(const AttnParams& ap, int grid, cudaStream_t stream) {
   cudaLaunchConfig_t cfg{};
-  cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(256);
+  cfg.gridDim = dim3(grid, kTileRows / 16);
+  cfg.blockDim = dim3(16 * DH / 8);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
@@ -990,7 +991,7 @@ cudaError_t launch_attention(const AttnHost& h, cudaStream_t stream, char* msg, 
   pp.max_block_len = h.max_block_len;
   pp.blk_tile = h.precise ? 64 : kTileKeys;
   cudaError_t e = cudaSuccess;
-  int64_t nr_blocks = (h.total_q + 7) / 8;
+  int64_t nr_blocks = (h.total_q * norm_rope_items_per_token(pp.job, h.dh) + 7) / 8;
   nr_blocks = std::min<int64_t>(nr_blocks, static_cast<int64_t>(h.num_sms) * 2);  // all co-resident
   const unsigned grid_a = static_cast<unsigned>(1 + nr_blocks);
   if (h.dh == 128)
@@ -1037,8 +1038,14 @@ cudaError_t launch_attention(const AttnHost& h, cudaStream_t stream, char* msg, 
   ap.grid = h.grid;
   const int grid_b = h.grid;
   // ---- B: attention
+  // K/V ring split for Dh = 128 (five 32 KB stages): DFLASH_RING=23 selects 2 K + 3 V stages
+  static const bool ring23 = [] {
+    const char* e = std::getenv("DFLASH_RING");
+    return e != nullptr && std::strcmp(e, "23") == 0;
+  }();
   if (h.dh == 128)
     e = h.precise ? launch_b<128, 2, 2, 1, true>(tq, tkc, tvc, tkb, tvb, tql, tkbl, ap, grid_b, stream)
+        : ring23  ? launch_b<128, 2, 3, 2, false>(tq, tkc, tvc, tkb, tvb, tql, tkbl, ap, grid_b, stream)
                   : launch_b<128, 3, 2, 2, false>(tq, tkc, tvc, tkb, tvb, tql, tkbl, ap, grid_b, stream);
   else
     e = h.precise ? launch_b<64, 3, 3, 2, true>(tq, tkc, tvc, tkb, tvb, tql, tkbl, ap, grid_b, stream)

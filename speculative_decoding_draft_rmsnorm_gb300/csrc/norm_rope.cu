@@ -26,9 +26,9 @@ __global__ void __launch_bounds__(256) norm_rope_kernel(const __grid_constant__ 
 
 cudaError_t launch_norm_rope(const NormRopeJob& job, int dh, int num_sms, cudaStream_t stream) {
   if (job.n_tok <= 0) return cudaSuccess;
-  const int64_t warps_needed = job.n_tok;
+  const int64_t warps_needed = job.n_tok * norm_rope_items_per_token(job, dh);
   int64_t blocks = (warps_needed + 7) / 8;
-  const int64_t cap = static_cast<int64_t>(num_sms) * 8;  // 8 blocks x 8 warps resident per SM
+  const int64_t cap = static_cast<int64_t>(num_sms) * 4;  // a few waves of 8-warp blocks per SM
   if (blocks > cap) blocks = cap;
   if (dh == 128) {
     norm_rope_kernel<128><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(job);

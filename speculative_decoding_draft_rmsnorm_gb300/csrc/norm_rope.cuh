@@ -39,11 +39,16 @@ __device__ __forceinline__ float rope_turns(int pos, float hi, float lo) {
   return t - rintf(t);
 }
 
+// Work item: one token and a chunk of up to RPS * kUnroll of its heads in one part. The
+// chunk's loads (and V loads) are all issued before any arithmetic, so a warp keeps
+// kUnroll 16-byte loads per lane in flight; items are spread over all warps of the grid.
 template <int DH>
 __device__ __forceinline__ void norm_rope_rows(const NormRopeJob& job, int64_t warp_id, int64_t n_warps) {
   constexpr int LR = DH / 8;       // lanes per row
   constexpr int HL = LR / 2;       // lanes per half row
   constexpr int RPS = 32 / LR;     // rows per warp step
+  constexpr int kUnroll = 4;       // warp steps per item
+  constexpr int HPI = RPS * kUnroll;  // heads per item
   const int lane = threadIdx.x & 31;
   const int sub = lane % LR;
   const int half = sub / HL;
@@ -52,109 +57,106 @@ __device__ __forceinline__ void norm_rope_rows(const NormRopeJob& job, int64_t w
   const int pelem0 = (1 - half) * (DH / 2) + 8 * q;  // partner's elements
   const int row_in_step = lane / LR;
   const float sgn = half ? 1.0f : -1.0f;
-
-  // weights of this lane's and the partner's elements, per part
-  float w_me[2][8], w_pa[2][8];
-#pragma unroll
-  for (int p = 0; p < 2; ++p) {
-    if (p < job.nparts) {
-      const uint4 a = *reinterpret_cast<const uint4*>(job.part[p].w + elem0);
-      const uint4 b = *reinterpret_cast<const uint4*>(job.part[p].w + pelem0);
-      const uint32_t av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        w_me[p][2 * e] = bf16lo_to_f32(av[e]);
-        w_me[p][2 * e + 1] = bf16hi_to_f32(av[e]);
-        w_pa[p][2 * e] = bf16lo_to_f32(bv[e]);
-        w_pa[p][2 * e + 1] = bf16hi_to_f32(bv[e]);
-      }
-    } else {
-#pragma unroll
-      for (int e = 0; e < 8; ++e) w_me[p][e] = w_pa[p][e] = 0.0f;
-    }
-  }
+  const float inv_dh = 1.0f / static_cast<float>(DH);
   float thi[8], tlo[8];
 #pragma unroll
   for (int e = 0; e < 8; ++e) {
     thi[e] = job.turns.hi[8 * q + e];
     tlo[e] = job.turns.lo[8 * q + e];
   }
-  const float inv_dh = 1.0f / static_cast<float>(DH);
+  const int chunks0 = (job.part[0].heads + HPI - 1) / HPI;
+  const int chunks1 = job.nparts > 1 ? (job.part[1].heads + HPI - 1) / HPI : 0;
+  const int cpt = chunks0 + chunks1;  // items per token
+  const int64_t n_items = job.n_tok * cpt;
 
-  for (int64_t t = warp_id; t < job.n_tok; t += n_warps) {
+  for (int64_t item = warp_id; item < n_items; item += n_warps) {
+    const int64_t t = item / cpt;
+    const int c = static_cast<int>(item - t * cpt);
+    const int p = c < chunks0 ? 0 : 1;
+    const NormRopePart& P = job.part[p];
+    const int hc = (p == 0 ? c : c - chunks0) * HPI;
     int64_t dst_row = t;
     if (job.slot) {
-      const int32_t s = job.slot[t];
-      if (s < 0 || s >= job.capacity) {
+      const int32_t sl = job.slot[t];
+      if (sl < 0 || sl >= job.capacity) {
         if (lane == 0 && job.err) atomicOr(job.err, kErrMetadata);
         continue;
       }
-      dst_row = s;
+      dst_row = sl;
+    }
+    // issue every load of the item first
+    uint4 raw[kUnroll], vraw[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int h = hc + u * RPS + row_in_step;
+      raw[u] = make_uint4(0, 0, 0, 0);
+      vraw[u] = make_uint4(0, 0, 0, 0);
+      if (h < P.heads) {
+        raw[u] = *reinterpret_cast<const uint4*>(P.src + (t * P.heads + h) * DH + elem0);
+        if (P.v_src) vraw[u] = *reinterpret_cast<const uint4*>(P.v_src + (t * P.heads + h) * DH + elem0);
+      }
+    }
+    float w_me[8], w_pa[8];
+    {
+      const uint4 a = *reinterpret_cast<const uint4*>(P.w + elem0);
+      const uint4 b = *reinterpret_cast<const uint4*>(P.w + pelem0);
+      const uint32_t av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        w_me[2 * e] = bf16lo_to_f32(av[e]);
+        w_me[2 * e + 1] = bf16hi_to_f32(av[e]);
+        w_pa[2 * e] = bf16lo_to_f32(bv[e]);
+        w_pa[2 * e + 1] = bf16hi_to_f32(bv[e]);
+      }
     }
     const int pos = job.pos[t];
-    float c[8], s[8];
+    float cs[8], sn[8];
 #pragma unroll
-    for (int e = 0; e < 8; ++e) sincospif(2.0f * rope_turns(pos, thi[e], tlo[e]), &s[e], &c[e]);
+    for (int e = 0; e < 8; ++e) sincospif(2.0f * rope_turns(pos, thi[e], tlo[e]), &sn[e], &cs[e]);
 
 #pragma unroll
-    for (int p = 0; p < 2; ++p) {
-      if (p >= job.nparts) break;
-      const NormRopePart& P = job.part[p];
-      for (int h0 = 0; h0 < P.heads; h0 += RPS) {
-        const int h = h0 + row_in_step;
-        const bool active = h < P.heads;
-        const int64_t src_off = (t * P.heads + (active ? h : 0)) * DH;
-        uint4 raw = make_uint4(0, 0, 0, 0);
-        if (active) raw = *reinterpret_cast<const uint4*>(P.src + src_off + elem0);
-        float x[8];
-        {
-          const uint32_t rv[4] = {raw.x, raw.y, raw.z, raw.w};
+    for (int u = 0; u < kUnroll; ++u) {
+      const int h = hc + u * RPS + row_in_step;
+      float x[8], xp[8];
+      {
+        const uint32_t rv[4] = {raw[u].x, raw[u].y, raw[u].z, raw[u].w};
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            x[2 * e] = bf16lo_to_f32(rv[e]);
-            x[2 * e + 1] = bf16hi_to_f32(rv[e]);
-          }
+        for (int e = 0; e < 4; ++e) {
+          x[2 * e] = bf16lo_to_f32(rv[e]);
+          x[2 * e + 1] = bf16hi_to_f32(rv[e]);
         }
-        float ss = 0.0f;
+      }
+      float ss = 0.0f;
 #pragma unroll
-        for (int e = 0; e < 8; ++e) ss = fmaf(x[e], x[e], ss);
+      for (int e = 0; e < 8; ++e) ss = fmaf(x[e], x[e], ss);
 #pragma unroll
-        for (int o = 1; o < LR; o <<= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-        const float rs = rsqrtf(fmaf(ss, inv_dh, job.eps));
-        uint4 praw;
-        praw.x = __shfl_xor_sync(0xffffffffu, raw.x, HL);
-        praw.y = __shfl_xor_sync(0xffffffffu, raw.y, HL);
-        praw.z = __shfl_xor_sync(0xffffffffu, raw.z, HL);
-        praw.w = __shfl_xor_sync(0xffffffffu, raw.w, HL);
-        float xp[8];
-        {
-          const uint32_t rv[4] = {praw.x, praw.y, praw.z, praw.w};
+      for (int o = 1; o < LR; o <<= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+      const float rs = rsqrtf(fmaf(ss, inv_dh, job.eps));
+      {
+        const uint32_t rv[4] = {__shfl_xor_sync(0xffffffffu, raw[u].x, HL), __shfl_xor_sync(0xffffffffu, raw[u].y, HL),
+                                __shfl_xor_sync(0xffffffffu, raw[u].z, HL), __shfl_xor_sync(0xffffffffu, raw[u].w, HL)};
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            xp[2 * e] = bf16lo_to_f32(rv[e]);
-            xp[2 * e + 1] = bf16hi_to_f32(rv[e]);
-          }
+        for (int e = 0; e < 4; ++e) {
+          xp[2 * e] = bf16lo_to_f32(rv[e]);
+          xp[2 * e + 1] = bf16hi_to_f32(rv[e]);
         }
-        uint32_t ohi[4], olo[4];
+      }
+      uint32_t ohi[4], olo[4];
 #pragma unroll
-        for (int e = 0; e < 8; e += 2) {
-          const float y0 = x[e] * rs * w_me[p][e], y1 = x[e + 1] * rs * w_me[p][e + 1];
-          const float z0 = xp[e] * rs * w_pa[p][e], z1 = xp[e + 1] * rs * w_pa[p][e + 1];
-          const float o0 = fmaf(sgn * z0, s[e], y0 * c[e]);
-          const float o1 = fmaf(sgn * z1, s[e + 1], y1 * c[e + 1]);
-          const uint32_t hi = pack_bf16x2(o0, o1);
-          ohi[e / 2] = hi;
-          olo[e / 2] = pack_bf16x2(o0 - bf16lo_to_f32(hi), o1 - bf16hi_to_f32(hi));
-        }
-        if (active) {
-          const int64_t dst_off = (dst_row * P.heads + h) * DH + elem0;
-          *reinterpret_cast<uint4*>(P.dst_hi + dst_off) = make_uint4(ohi[0], ohi[1], ohi[2], ohi[3]);
-          if (P.dst_lo) *reinterpret_cast<uint4*>(P.dst_lo + dst_off) = make_uint4(olo[0], olo[1], olo[2], olo[3]);
-          if (P.v_src) {
-            const uint4 v = *reinterpret_cast<const uint4*>(P.v_src + src_off + elem0);
-            *reinterpret_cast<uint4*>(P.v_dst + dst_off) = v;
-          }
-        }
+      for (int e = 0; e < 8; e += 2) {
+        const float y0 = x[e] * rs * w_me[e], y1 = x[e + 1] * rs * w_me[e + 1];
+        const float z0 = xp[e] * rs * w_pa[e], z1 = xp[e + 1] * rs * w_pa[e + 1];
+        const float o0 = fmaf(sgn * z0, sn[e], y0 * cs[e]);
+        const float o1 = fmaf(sgn * z1, sn[e + 1], y1 * cs[e + 1]);
+        const uint32_t hi = pack_bf16x2(o0, o1);
+        ohi[e / 2] = hi;
+        olo[e / 2] = pack_bf16x2(o0 - bf16lo_to_f32(hi), o1 - bf16hi_to_f32(hi));
+      }
+      if (h < P.heads) {
+        const int64_t dst_off = (dst_row * P.heads + h) * DH + elem0;
+        *reinterpret_cast<uint4*>(P.dst_hi + dst_off) = make_uint4(ohi[0], ohi[1], ohi[2], ohi[3]);
+        if (P.dst_lo) *reinterpret_cast<uint4*>(P.dst_lo + dst_off) = make_uint4(olo[0], olo[1], olo[2], olo[3]);
+        if (P.v_src) *reinterpret_cast<uint4*>(P.v_dst + dst_off) = vraw[u];
       }
     }
   }
