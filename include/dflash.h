@@ -169,6 +169,32 @@ DFLASH_API int dflash_block_attention(const dflash_bf16* q_raw, const dflash_bf1
                            size_t workspace_bytes, int flags, dflash_stream_t stream);
 
 /*
+ * dflash_block_attention_noalloc -- dflash_block_attention without a caller workspace.
+ * The pages have no counterpart: this entry point exists for callers that cannot
+ * allocate device memory themselves (a plugin host that owns every byte of device
+ * memory, code running inside another allocator's callback, deployments with a static
+ * memory plan where a run-time cudaMalloc is not allowed). Arguments are those of
+ * dflash_block_attention minus the workspace; inputs and output are still the caller's.
+ * The scratch is a 32 MiB array compiled into the library: every GPU that loads the
+ * library holds it until the process exits. A call whose workspace would exceed 32 MiB
+ * (dflash_block_attention_workspace_size) fails with DFLASH_ERR_WORKSPACE and does
+ * nothing. The first call on a device looks up the array's device address with that
+ * device current and caches it; make that first call before any stream capture. All
+ * calls on a device share the array, so calls that overlap on the GPU (two streams at
+ * once) race and must not be issued. dflash_check_error cannot read this scratch; errors
+ * of the call itself are returned and described by dflash_last_error.
+ */
+DFLASH_API int dflash_block_attention_noalloc(const dflash_bf16* q_raw, const dflash_bf16* k_blk,
+                                              const dflash_bf16* v_blk, const dflash_bf16* ctx_k,
+                                              const dflash_bf16* ctx_v, const int32_t* query_start_loc,
+                                              const int32_t* ctx_start_loc, const int32_t* ctx_lens,
+                                              const int32_t* positions, const dflash_bf16* q_norm_w,
+                                              const dflash_bf16* k_norm_w, int num_reqs, int64_t total_q, int hq,
+                                              int hkv, int dh, int64_t total_ctx, int max_ctx_len, int max_block_len,
+                                              float eps, float rope_theta, float scale, int causal, int window,
+                                              int out_dtype, void* out, int flags, dflash_stream_t stream);
+
+/*
  * Reads the device error word the last dflash_block_attention call on this workspace
  * left (waits for `stream`). Returns DFLASH_OK, DFLASH_ERR_DEVICE_TIMEOUT or
  * DFLASH_ERR_DEVICE_METADATA; the word is cleared by the next attention call.
