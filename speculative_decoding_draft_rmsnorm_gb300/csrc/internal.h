@@ -50,6 +50,15 @@ struct NormRopeJob {
 
 cudaError_t launch_norm_rope(const NormRopeJob& job, int dh, int num_sms, cudaStream_t stream);
 
+// Work items (warp tasks) per token of a norm+rope job: heads are taken in chunks of
+// 4 * 32 / (Dh / 8) per item.
+inline int norm_rope_items_per_token(const NormRopeJob& job, int dh) {
+  const int hpi = 4 * (32 / (dh / 8));
+  int n = (job.part[0].heads + hpi - 1) / hpi;
+  if (job.nparts > 1) n += (job.part[1].heads + hpi - 1) / hpi;
+  return n;
+}
+
 // One group of the attention kernel's work: (request, kv head, query tile) with its n key
 // tiles (context tiles first, then block tiles) at global tile indices [start, start+n).
 struct Group {
