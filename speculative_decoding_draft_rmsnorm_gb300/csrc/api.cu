@@ -242,6 +242,7 @@ int dflash_block_attention(const dflash_bf16* q_raw, const dflash_bf16* k_blk, c
   h.k_hat = reinterpret_cast<uint16_t*>(ws + w.k_hat);
   h.k_lo = precise ? reinterpret_cast<uint16_t*>(ws + w.k_lo) : nullptr;
   h.groups = reinterpret_cast<dflash::Group*>(ws + w.groups);
+  h.cta_rec = w.balanced ? reinterpret_cast<dflash::CtaRecord*>(ws + w.cta_rec) : nullptr;
   h.part_o = w.balanced ? reinterpret_cast<float*>(ws + w.part_o) : nullptr;
   h.part_ml = w.balanced ? reinterpret_cast<float*>(ws + w.part_ml) : nullptr;
   dflash::make_rope_turns(dh, static_cast<double>(rope_theta), &h.turns);

@@ -46,6 +46,8 @@ struct PrologueParams {
   NormRopeJob job;
   const int32_t *qsl, *csl, *clen;
   Group* groups;
+  CtaRecord* cta_rec;  // balanced schedule: one record per CTA of kernel B (else null)
+  int grid_b;          // CTAs of kernel B
   uint32_t* hdr;
   int64_t total_q, total_ctx;
   int num_reqs, hkv, g, tpq, causal, window;
@@ -53,105 +55,215 @@ struct PrologueParams {
   int blk_tile;  // keys per block-key tile: 128, or 64 when hi and lo halves share a tile
 };
 
+__device__ __forceinline__ void load_group(const Group* groups, int g, Group& G) {
+  const int4* src = reinterpret_cast<const int4*>(groups + g);
+  int4* dst = reinterpret_cast<int4*>(&G);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) dst[i] = src[i];
+}
+
+struct ReqTiles {  // one request's share of the group table
+  int r, cnt, QT, n, C, B, lo, nct, c0, q0, goff;
+  long long toff;
+};
+
+__device__ __forceinline__ Group make_group(const ReqTiles& q, int k, int tpq, int g) {
+  Group G;
+  G.r = q.r;
+  G.kvh = k / q.QT;
+  G.qt = k % q.QT;
+  G.n = q.n;
+  G.start = static_cast<int>(q.toff + static_cast<long long>(k) * q.n);
+  G.clen = q.C;
+  G.blen = q.B;
+  G.ctx_lo = q.lo;
+  G.n_ctx_tiles = q.nct;
+  G.csl = q.c0;
+  G.qsl = q.q0;
+  G.tok0 = G.qt * tpq;
+  G.rows = min(tpq, q.B - G.tok0) * g;
+  G.pad0 = G.pad1 = G.pad2 = 0;
+  return G;
+}
+
+// floor(c * T / grid) for 0 <= c <= grid, T < 2^31: 32-bit division when the product fits
+__device__ __forceinline__ long long cta_first_tile(long long c, long long T, long long grid) {
+  const unsigned long long prod = static_cast<unsigned long long>(c) * static_cast<unsigned long long>(T);
+  if (prod <= 0xffffffffull) return static_cast<unsigned>(prod) / static_cast<unsigned>(grid);
+  return static_cast<long long>(prod / static_cast<unsigned long long>(grid));
+}
+
 // Validates the device metadata and writes one Group per (request, kv head, query tile)
 // with its key-tile count and the global index of its first tile (prefix over groups).
-// hdr[1] = number of groups, hdr[2] = total tiles.
+// hdr[1] = number of groups, hdr[2] = total tiles. For the balanced schedule it also
+// writes each CTA's record: CTA c owns tiles [c*T/grid, (c+1)*T/grid), its first group is
+// the one holding tile c*T/grid, and the record carries that group so that the CTA's
+// first loads depend on one read.
+//
+// One block of 256 threads. Requests are taken 256 at a time: a thread loads its request's
+// metadata (one round trip), the block scans the group and tile counts, then every thread
+// writes the groups gi = tid, tid + 256, ... of the chunk (its request found by a search
+// over the scan in shared memory) and, with one chunk, one thread per CTA writes the CTA's
+// record, so no thread walks a request's groups serially.
 __device__ void build_groups(const PrologueParams& p) {
-  __shared__ int s_cnt[256];
-  __shared__ long long s_til[256];
+  __shared__ ReqTiles s_req[256];
+  __shared__ int s_cnt[256];  // inclusive scan of the chunk's group counts
+  __shared__ int s_wg[8];
+  __shared__ long long s_wt[8];
   __shared__ int s_bad_global;
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   if (tid == 0) {
     p.hdr[0] = 0;  // error word of this call (only this block writes it before kernel B)
-    int bad = 0;
-    if (p.num_reqs > 0 && (p.qsl[0] != 0 || p.qsl[p.num_reqs] != p.total_q)) bad = 1;
-    s_bad_global = bad;
-    if (bad) atomicOr(&p.hdr[0], kErrMetadata);
+    s_bad_global = 0;
   }
   __syncthreads();
-  const bool bad_global = s_bad_global != 0;
+  const bool one_chunk = p.num_reqs <= 256;
+  const long long grid = p.grid_b;
   int run_g = 0;
   long long run_t = 0;
   for (int base = 0; base < p.num_reqs; base += 256) {
-    const int r = base + tid;
-    int cnt = 0, B = 0, C = 0, lo = 0, nct = 0, n = 0, QT = 0, c0 = 0, q0 = 0;
-    if (r < p.num_reqs && !bad_global) {
-      q0 = p.qsl[r];
-      const int q1 = p.qsl[r + 1];
-      c0 = p.csl[r];
-      const int c1 = p.csl[r + 1];
-      B = q1 - q0;
-      C = p.clen[r];
-      const bool ok = B >= 0 && q0 >= 0 && q1 <= p.total_q && c0 >= 0 && c1 >= c0 && c1 <= p.total_ctx && C >= 0 &&
-                      C <= c1 - c0 && C <= p.max_ctx_len && B <= p.max_block_len;
+    ReqTiles q{};
+    q.r = base + tid;
+    if (q.r < p.num_reqs) {
+      // all loads of the request are independent: one round trip
+      q.q0 = p.qsl[q.r];
+      const int q1 = p.qsl[q.r + 1];
+      q.c0 = p.csl[q.r];
+      const int c1 = p.csl[q.r + 1];
+      q.C = p.clen[q.r];
+      q.B = q1 - q.q0;
+      if ((q.r == 0 && q.q0 != 0) || (q.r == p.num_reqs - 1 && q1 != p.total_q)) s_bad_global = 1;
+      const bool ok = q.B >= 0 && q.q0 >= 0 && q1 <= p.total_q && q.c0 >= 0 && c1 >= q.c0 && c1 <= p.total_ctx &&
+                      q.C >= 0 && q.C <= c1 - q.c0 && q.C <= p.max_ctx_len && q.B <= p.max_block_len;
       if (!ok) {
         atomicOr(&p.hdr[0], kErrMetadata);
-        B = 0;
+        q.B = 0;
       }
-      if (B > 0) {
-        lo = (p.causal && p.window > 0) ? max(0, C - p.window + 1) : 0;
-        nct = (C - lo + kTileKeys - 1) / kTileKeys;
-        n = nct + (B + p.blk_tile - 1) / p.blk_tile;
-        QT = (B + p.tpq - 1) / p.tpq;
-        cnt = p.hkv * QT;
+      if (q.B > 0) {
+        q.lo = (p.causal && p.window > 0) ? max(0, q.C - p.window + 1) : 0;
+        q.nct = (q.C - q.lo + kTileKeys - 1) / kTileKeys;
+        q.n = q.nct + (q.B + p.blk_tile - 1) / p.blk_tile;
+        q.QT = (q.B + p.tpq - 1) / p.tpq;
+        q.cnt = p.hkv * q.QT;
       }
     }
-    // block-wide inclusive scans of the group and tile counts
-    s_cnt[tid] = cnt;
-    s_til[tid] = static_cast<long long>(cnt) * n;
-    __syncthreads();
-    for (int off = 1; off < 256; off <<= 1) {
-      const int vc = tid >= off ? s_cnt[tid - off] : 0;
-      const long long vt = tid >= off ? s_til[tid - off] : 0;
-      __syncthreads();
-      s_cnt[tid] += vc;
-      s_til[tid] += vt;
-      __syncthreads();
-    }
-    const int goff = run_g + s_cnt[tid] - cnt;
-    const long long toff = run_t + s_til[tid] - static_cast<long long>(cnt) * n;
-    const int chunk_g = s_cnt[255];
-    const long long chunk_t = s_til[255];
-    __syncthreads();
-    for (int k = 0; k < cnt; ++k) {
-      const int gi = goff + k;
-      if (gi >= p.groups_max) {
-        atomicOr(&p.hdr[0], kErrMetadata);
-        break;
+    // block-wide inclusive scans of the group and tile counts: warp shuffles, then warp totals
+    int ic = q.cnt;
+    long long it = static_cast<long long>(q.cnt) * q.n;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int vc = __shfl_up_sync(0xffffffffu, ic, off);
+      const long long vt = __shfl_up_sync(0xffffffffu, it, off);
+      if (lane >= off) {
+        ic += vc;
+        it += vt;
       }
-      Group G;
-      G.r = r;
-      G.kvh = k / QT;
-      G.qt = k % QT;
-      G.n = n;
-      G.start = static_cast<int>(toff + static_cast<long long>(k) * n);
-      G.clen = C;
-      G.blen = B;
-      G.ctx_lo = lo;
-      G.n_ctx_tiles = nct;
-      G.csl = c0;
-      G.qsl = q0;
-      G.tok0 = G.qt * p.tpq;
-      G.rows = min(p.tpq, B - G.tok0) * p.g;
-      G.pad0 = G.pad1 = G.pad2 = 0;
-      p.groups[gi] = G;
+    }
+    if (lane == 31) {
+      s_wg[wid] = ic;
+      s_wt[wid] = it;
+    }
+    __syncthreads();
+    int wg_before = 0, chunk_g = 0;
+    long long wt_before = 0, chunk_t = 0;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) {
+      if (w < wid) {
+        wg_before += s_wg[w];
+        wt_before += s_wt[w];
+      }
+      chunk_g += s_wg[w];
+      chunk_t += s_wt[w];
+    }
+    ic += wg_before;
+    it += wt_before;
+    q.goff = run_g + ic - q.cnt;
+    q.toff = run_t + it - static_cast<long long>(q.cnt) * q.n;
+    s_cnt[tid] = ic;
+    s_req[tid] = q;
+    __syncthreads();
+    const bool fits = run_g + chunk_g <= p.groups_max && run_t + chunk_t <= 0x7fffffffLL;
+    if (!fits && tid == 0) atomicOr(&p.hdr[0], kErrMetadata);
+    for (int j = tid; fits && j < chunk_g; j += blockDim.x) {
+      int a = 0, b = 255;  // first request of the chunk whose inclusive count exceeds j
+      while (a < b) {
+        const int m = (a + b) >> 1;
+        if (s_cnt[m] > j) b = m; else a = m + 1;
+      }
+      const ReqTiles& rq = s_req[a];
+      const int gi = run_g + j;
+      p.groups[gi] = make_group(rq, gi - rq.goff, p.tpq, p.g);
+    }
+    if (one_chunk && fits && p.cta_rec != nullptr && chunk_t > 0) {
+      // one thread per CTA: its range, the request holding its first tile (the last request
+      // whose first tile is <= lo: that one has groups), and the group within it
+      for (int c = tid; c < grid; c += blockDim.x) {
+        const long long lo = cta_first_tile(c, chunk_t, grid), hi = cta_first_tile(c + 1, chunk_t, grid);
+        int a = 0, z = p.num_reqs - 1;
+        while (a < z) {
+          const int m = (a + z + 1) >> 1;
+          if (s_req[m].toff <= lo) a = m; else z = m - 1;
+        }
+        const ReqTiles& rq = s_req[a];
+        const int k =
+            rq.n > 0 ? static_cast<int>(static_cast<unsigned>(lo - rq.toff) / static_cast<unsigned>(rq.n)) : 0;
+        CtaRecord rec;
+        rec.first = make_group(rq, k, p.tpq, p.g);
+        rec.g0 = rq.goff + k;
+        rec.lo = static_cast<int>(lo);
+        rec.hi = static_cast<int>(hi);
+        rec.ng = chunk_g;
+        p.cta_rec[c] = rec;
+      }
     }
     run_g += chunk_g;
     run_t += chunk_t;
+    __syncthreads();  // s_req and s_cnt are rewritten by the next chunk
+  }
+  if (s_bad_global || run_g > p.groups_max || run_t > 0x7fffffffLL) {
+    // no work for kernel B (the last two cannot happen with valid host bounds)
+    if (tid == 0) atomicOr(&p.hdr[0], kErrMetadata);
+    run_g = 0;
+    run_t = 0;
   }
   if (tid == 0) {
-    if (run_g > p.groups_max || run_t > 0x7fffffffLL) {  // cannot happen with valid host bounds
-      atomicOr(&p.hdr[0], kErrMetadata);
-      run_g = 0;
-      run_t = 0;
-    }
     p.hdr[1] = static_cast<uint32_t>(run_g);
     p.hdr[2] = static_cast<uint32_t>(run_t);
   }
+  if (p.cta_rec == nullptr) return;
+  if (run_t == 0) {
+    // records written above (if any) are replaced: no CTA has work
+    for (int c = tid; c < grid; c += blockDim.x) p.cta_rec[c] = CtaRecord{};
+    return;
+  }
+  if (!one_chunk) {
+    // several chunks: the total is known only now; read the table back (this block wrote
+    // it, and the barrier at the end of the last chunk made it visible to all its threads)
+    for (int gi = tid; gi < run_g; gi += blockDim.x) {
+      Group G;
+      load_group(p.groups, gi, G);
+      const long long st = G.start;
+      // the CTAs whose first tile lies in [st, st + n): ceil(st*grid/T) .. ceil((st+n)*grid/T) - 1
+      const long long c0 = (st * grid + run_t - 1) / run_t;
+      long long c1 = ((st + G.n) * grid + run_t - 1) / run_t - 1;
+      if (c1 > grid - 1) c1 = grid - 1;
+      for (long long c = c0; c <= c1; ++c) {
+        CtaRecord rec;
+        rec.first = G;
+        rec.g0 = gi;
+        rec.lo = static_cast<int>(cta_first_tile(c, run_t, grid));
+        rec.hi = static_cast<int>(cta_first_tile(c + 1, run_t, grid));
+        rec.ng = run_g;
+        p.cta_rec[c] = rec;
+      }
+    }
+  }
 }
 
+// Three blocks per SM (at most 85 registers a thread), so that the launch below, sized to
+// one item per warp where it can be, is resident at once.
 template <int DH>
-__global__ void __launch_bounds__(256) prologue_kernel(const __grid_constant__ PrologueParams p) {
+__global__ void __launch_bounds__(256, 3) prologue_kernel(const __grid_constant__ PrologueParams p) {
   grid_dependents_launch();
   if (blockIdx.x == 0) {
     build_groups(p);
@@ -159,7 +271,7 @@ __global__ void __launch_bounds__(256) prologue_kernel(const __grid_constant__ P
   }
   const int64_t warp_id = (static_cast<int64_t>(blockIdx.x - 1) * blockDim.x + threadIdx.x) >> 5;
   const int64_t n_warps = (static_cast<int64_t>(gridDim.x - 1) * blockDim.x) >> 5;
-  norm_rope_rows<DH>(p.job, warp_id, n_warps);
+  norm_rope_rows<DH, false>(p.job, warp_id, n_warps);
 }
 
 // ================================================================ kernel B
@@ -186,12 +298,14 @@ struct Layout {
   static constexpr int DRAIN = Q_FULL + 14;  // final commit of the MMA thread (its own barrier)
   static constexpr int NBARS = Q_FULL + 15;
   static constexpr int OFF_MISC = OFF_BAR + NBARS * 8;
-  static constexpr int BYTES = OFF_MISC + 64;
+  static constexpr int OFF_REC = (OFF_MISC + 64 + 15) / 16 * 16;  // CtaRecord (80 bytes)
+  static constexpr int BYTES = OFF_REC + 80;
   static constexpr int ALLOC = BYTES + 1024;
 };
 
 struct AttnParams {
   const Group* groups;
+  const CtaRecord* cta_rec;  // balanced schedule
   uint32_t* hdr;
   float* part_o;
   float* part_ml;
@@ -227,13 +341,6 @@ __device__ __forceinline__ TileInfo tile_info(const Group& U, int t, int blk_til
   return ti;
 }
 
-__device__ __forceinline__ void load_group(const Group* groups, int g, Group& G) {
-  const int4* src = reinterpret_cast<const int4*>(groups + g);
-  int4* dst = reinterpret_cast<int4*>(&G);
-#pragma unroll
-  for (int i = 0; i < 4; ++i) dst[i] = src[i];
-}
-
 // One segment of a CTA's work: key tiles [t0, t1) of one group.
 struct Seg {
   Group grp;
@@ -246,13 +353,17 @@ struct Seg {
 // same sequence.
 struct SegIter {
   const Group* groups;
-  long long lo, hi;  // balanced: this CTA's tile range
+  const Group* first;  // balanced: the first group, from the CTA record (shared memory)
+  long long lo, hi;    // balanced: this CTA's tile range
   int ng, g, k;
   bool balanced;
   __device__ bool next(Seg& s) {
     if (balanced) {
       if (lo >= hi || g >= ng) return false;
-      load_group(groups, g, s.grp);
+      if (k == 0)
+        s.grp = *first;
+      else
+        load_group(groups, g, s.grp);
       if (s.grp.start >= hi) return false;
       const long long st = s.grp.start;
       s.t0 = static_cast<int>((lo > st ? lo : st) - st);
@@ -337,41 +448,22 @@ attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
 
   grid_dependency_wait();  // group table and q^/k^ come from the prologue kernel
   grid_dependents_launch();
-  long long* s_range = reinterpret_cast<long long*>(smem + L::OFF_MISC + 16);
-  int* s_first = reinterpret_cast<int*>(smem + L::OFF_MISC + 32);
-  if (tid == 0) {
-    const int ng = static_cast<int>(p.hdr[1]);
-    const long long tt = static_cast<long long>(p.hdr[2]);
-    long long lo = 0, hi = 0;
-    int g0 = blockIdx.x;
-    if (p.balanced) {
-      lo = static_cast<long long>(blockIdx.x) * tt / gridDim.x;
-      hi = static_cast<long long>(blockIdx.x + 1) * tt / gridDim.x;
-      int a = 0, b = ng - 1;  // last group whose first tile is <= lo
-      g0 = 0;
-      while (a <= b) {
-        const int m = (a + b) >> 1;
-        if (p.groups[m].start <= lo) {
-          g0 = m;
-          a = m + 1;
-        } else {
-          b = m - 1;
-        }
-      }
-    }
-    s_range[0] = lo;
-    s_range[1] = hi;
-    s_first[0] = g0;
-    s_first[1] = ng;
+  // balanced: this CTA's record (first group, g0, lo, hi, ng); else g0 = blockIdx.x, ng
+  int4* s_rec = reinterpret_cast<int4*>(smem + L::OFF_REC);
+  if (p.balanced) {
+    if (tid < 5) s_rec[tid] = reinterpret_cast<const int4*>(p.cta_rec + blockIdx.x)[tid];
+  } else if (tid == 0) {
+    s_rec[4] = make_int4(static_cast<int>(blockIdx.x), 0, 0, static_cast<int>(p.hdr[1]));
   }
   __syncthreads();
   auto make_iter = [&]() {
     SegIter it;
     it.groups = p.groups;
-    it.lo = s_range[0];
-    it.hi = s_range[1];
-    it.g = s_first[0];
-    it.ng = s_first[1];
+    it.first = reinterpret_cast<const Group*>(s_rec);
+    it.lo = s_rec[4].y;
+    it.hi = s_rec[4].z;
+    it.g = s_rec[4].x;
+    it.ng = s_rec[4].w;
     it.k = 0;
     it.balanced = p.balanced != 0;
     return it;
@@ -762,43 +854,78 @@ attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
 }
 
 // ================================================================ kernel C
+// One block per CTA boundary b (between CTAs b and b+1 of the attention kernel) and
+// 16-row slice: the group holding the boundary's tile is CTA b+1's first group, split
+// if it starts before CTA b+1's first tile. A group split by several boundaries is merged
+// by the block of its first one. The records come from the prologue, which completed
+// before the attention kernel passed its own dependency wait and let this grid launch,
+// so they are read before this grid's wait, which only the partials need.
 template <int DH>
 __global__ void __launch_bounds__(256) combine_kernel(const __grid_constant__ AttnParams p) {
-  grid_dependency_wait();
-  const int gi = blockIdx.x;
-  const int ng = static_cast<int>(p.hdr[1]);
-  const long long tt = static_cast<long long>(p.hdr[2]);
-  if (gi >= ng || !p.balanced || tt <= 0) return;
+  const int b = blockIdx.x;  // boundary between CTAs b and b + 1
   Group G;
-  load_group(p.groups, gi, G);
+  int lo1;
+  {
+    const CtaRecord* rec = p.cta_rec + b + 1;
+    const int4* src = reinterpret_cast<const int4*>(&rec->first);
+    int4* dst = reinterpret_cast<int4*>(&G);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) dst[i] = __ldcg(src + i);
+    lo1 = __ldcg(&rec->lo);
+  }
+  const long long tt = static_cast<long long>(__ldcg(p.hdr + 2));
   const long long grid = p.grid;
-  // CTA c of the attention kernel owned tiles [c*tt/grid, (c+1)*tt/grid)
+  const long long lo0 = static_cast<long long>(b) * tt / grid;  // CTA b's first tile
+  // split at this boundary, and not at an earlier one
+  const bool mine = tt > 0 && G.start < lo1 && G.start >= lo0;
+  grid_dependency_wait();
+  if (!mine) return;
+  // contributors: CTAs ca = b .. cb; the group is CTA b's first segment iff it starts at lo0
   auto cta_of = [&](long long t) { return ((t + 1) * grid + tt - 1) / tt - 1; };
-  const long long ca = cta_of(G.start), cb = cta_of(static_cast<long long>(G.start) + G.n - 1);
-  if (ca == cb) return;  // the group was finished by one CTA
-  const bool ca_first = ca * tt / grid >= G.start;  // the group is CTA ca's first segment
-  constexpr int CPR = DH / 8;  // 8-float chunks per row; block y covers rows [16y, 16y+16)
+  const long long ca = b, cb = cta_of(static_cast<long long>(G.start) + G.n - 1);
+  const bool ca_first = G.start == lo0;
+  constexpr int CPR = DH / 8;   // 8-float chunks per row; block y covers rows [16y, 16y+16)
+  constexpr int kMaxBatch = 2;  // contributors whose loads are in flight together
   for (int item = threadIdx.x; item < 16 * CPR; item += blockDim.x) {
     const int rho = 16 * static_cast<int>(blockIdx.y) + item / CPR;
     if (rho >= G.rows) break;
     const int c8 = (item % CPR) * 8;
-    float M = -INFINITY;
-    for (long long c = ca; c <= cb; ++c) {
-      const long long slot = 2 * c + ((c == ca && !ca_first) ? 1 : 0);
-      M = fmaxf(M, p.part_ml[(slot * kTileRows + rho) * 2]);
-    }
-    const float Me = M == -INFINITY ? 0.0f : M;
+    // running merge: o = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s, contributors in batches
+    float M = -INFINITY, L = 0.0f;
     float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-    float L = 0.0f;
-    for (long long c = ca; c <= cb; ++c) {
-      const long long slot = 2 * c + ((c == ca && !ca_first) ? 1 : 0);
-      const float* ml = p.part_ml + (slot * kTileRows + rho) * 2;
-      const float w = ml[0] == -INFINITY ? 0.0f : ex2_approx(ml[0] - Me);
-      L += w * ml[1];
-      const float4* src = reinterpret_cast<const float4*>(p.part_o + (slot * kTileRows + rho) * DH + c8);
-      const float4 a = src[0], b = src[1];
-      acc[0] += w * a.x; acc[1] += w * a.y; acc[2] += w * a.z; acc[3] += w * a.w;
-      acc[4] += w * b.x; acc[5] += w * b.y; acc[6] += w * b.z; acc[7] += w * b.w;
+    for (long long c = ca; c <= cb; c += kMaxBatch) {
+      float2 ml[kMaxBatch];
+      float4 oa[kMaxBatch], ob[kMaxBatch];
+#pragma unroll
+      for (int i = 0; i < kMaxBatch; ++i) {
+        const long long cc = c + i;
+        if (cc <= cb) {
+          const long long slot = 2 * cc + ((cc == ca && !ca_first) ? 1 : 0);
+          ml[i] = __ldcg(reinterpret_cast<const float2*>(p.part_ml + (slot * kTileRows + rho) * 2));
+          const float4* src = reinterpret_cast<const float4*>(p.part_o + (slot * kTileRows + rho) * DH + c8);
+          oa[i] = __ldcg(src);
+          ob[i] = __ldcg(src + 1);
+        } else {
+          ml[i] = make_float2(-INFINITY, 0.0f);
+          oa[i] = ob[i] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        }
+      }
+      float Mn = M;
+#pragma unroll
+      for (int i = 0; i < kMaxBatch; ++i) Mn = fmaxf(Mn, ml[i].x);
+      if (Mn == -INFINITY) continue;
+      const float r = M == -INFINITY ? 0.0f : ex2_approx(M - Mn);
+      L *= r;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) acc[e] *= r;
+#pragma unroll
+      for (int i = 0; i < kMaxBatch; ++i) {
+        const float w = ml[i].x == -INFINITY ? 0.0f : ex2_approx(ml[i].x - Mn);
+        L += w * ml[i].y;
+        acc[0] += w * oa[i].x; acc[1] += w * oa[i].y; acc[2] += w * oa[i].z; acc[3] += w * oa[i].w;
+        acc[4] += w * ob[i].x; acc[5] += w * ob[i].y; acc[6] += w * ob[i].z; acc[7] += w * ob[i].w;
+      }
+      M = Mn;
     }
     const float inv = L > 0.0f ? 1.0f / L : 0.0f;
     const int64_t tok = G.qsl + G.tok0 + rho / p.g;
@@ -914,6 +1041,8 @@ WorkspacePlan plan_workspace(int num_reqs, int64_t total_q, int hq, int hkv, int
   if (precise) off += align256(static_cast<size_t>(total_q) * hkv * dh * 2);
   w.groups = off;
   off += align256(static_cast<size_t>(w.groups_max) * sizeof(Group));
+  w.cta_rec = off;
+  if (w.balanced) off += align256(static_cast<size_t>(w.grid) * sizeof(CtaRecord));
   w.part_o = off;
   off += align256(static_cast<size_t>(w.parts) * kTileRows * dh * 4);
   w.part_ml = off;
@@ -977,6 +1106,8 @@ cudaError_t launch_attention(const AttnHost& h, cudaStream_t stream, char* msg, 
   pp.csl = h.csl;
   pp.clen = h.clen;
   pp.groups = h.groups;
+  pp.cta_rec = h.balanced ? h.cta_rec : nullptr;
+  pp.grid_b = h.grid;
   pp.hdr = h.ws_hdr;
   pp.total_q = h.total_q;
   pp.total_ctx = h.total_ctx;
@@ -992,7 +1123,7 @@ cudaError_t launch_attention(const AttnHost& h, cudaStream_t stream, char* msg, 
   pp.blk_tile = h.precise ? 64 : kTileKeys;
   cudaError_t e = cudaSuccess;
   int64_t nr_blocks = (h.total_q * norm_rope_items_per_token(pp.job, h.dh) + 7) / 8;
-  nr_blocks = std::min<int64_t>(nr_blocks, static_cast<int64_t>(h.num_sms) * 2);  // all co-resident
+  nr_blocks = std::min<int64_t>(nr_blocks, static_cast<int64_t>(h.num_sms) * 3 - 1);  // all co-resident
   const unsigned grid_a = static_cast<unsigned>(1 + nr_blocks);
   if (h.dh == 128)
     prologue_kernel<128><<<grid_a, 256, 0, stream>>>(pp);
@@ -1023,6 +1154,7 @@ cudaError_t launch_attention(const AttnHost& h, cudaStream_t stream, char* msg, 
   }
   AttnParams ap{};
   ap.groups = h.groups;
+  ap.cta_rec = h.cta_rec;
   ap.hdr = h.ws_hdr;
   ap.part_o = h.part_o;
   ap.part_ml = h.part_ml;
@@ -1052,11 +1184,11 @@ cudaError_t launch_attention(const AttnHost& h, cudaStream_t stream, char* msg, 
                   : launch_b<64, 4, 4, 2, false>(tq, tkc, tvc, tkb, tvb, tql, tkbl, ap, grid_b, stream);
   if (e != cudaSuccess) return e;
   // ---- C: combine split partials
-  if (h.balanced) {
+  if (h.balanced && h.grid > 1) {  // one block per CTA boundary and 16-row slice
     if (h.dh == 128)
-      e = launch_c<128>(ap, h.groups_max, stream);
+      e = launch_c<128>(ap, h.grid - 1, stream);
     else
-      e = launch_c<64>(ap, h.groups_max, stream);
+      e = launch_c<64>(ap, h.grid - 1, stream);
   }
   return e;
 }

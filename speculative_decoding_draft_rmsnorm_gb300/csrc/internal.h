@@ -69,6 +69,13 @@ struct Group {
 };
 static_assert(sizeof(Group) == 64, "group descriptor is 64 bytes");
 
+// Balanced schedule: what CTA c of the attention kernel needs before its first loads.
+struct CtaRecord {
+  Group first;         // the group holding the CTA's first tile
+  int g0, lo, hi, ng;  // its index; the CTA's tiles [lo, hi); the number of groups
+};
+static_assert(sizeof(CtaRecord) == 80, "CTA record is 80 bytes");
+
 struct AttnHost {
   // sizes
   int num_reqs, hq, hkv, dh, g, tpq, qt_max;
@@ -87,13 +94,14 @@ struct AttnHost {
   uint32_t* ws_hdr;   // [0] error word, [1] group count, [2] total key tiles
   uint16_t *q_hat, *q_lo, *k_hat, *k_lo;
   Group* groups;
+  CtaRecord* cta_rec; // [grid] balanced schedule only
   float* part_o;      // [2 * grid][64][dh]  partial O of straddling segments
   float* part_ml;     // [2 * grid][64][2]   their running max (log2 units) and weight sum
   RopeTurns turns;
 };
 
 struct WorkspacePlan {
-  size_t hdr, q_hat, q_lo, k_hat, k_lo, groups, part_o, part_ml, total;
+  size_t hdr, q_hat, q_lo, k_hat, k_lo, groups, cta_rec, part_o, part_ml, total;
   int groups_max, grid, parts, qt_max, tpq;
   double tiles_bound;
   bool balanced;

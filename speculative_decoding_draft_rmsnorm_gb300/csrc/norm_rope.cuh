@@ -14,7 +14,8 @@
 // elements [8q, 8q+8), lanes of the second half the partner elements [Dh/2 + 8q, ...),
 // so the rotation partner of a lane is lane ^ (Dh/16). 32 / (Dh/8) rows are processed
 // per warp step; the squared-norm reduction is a shuffle butterfly within the row's
-// lanes. The rotation angle of each lane's 8 frequencies is computed once per token.
+// lanes. All rows of a warp's item belong to one token, so each of the Dh/2 rotation
+// angles is computed by one lane (Dh/64 per lane) and fetched by the others with shuffles.
 //
 // Angle: turns = pos * (inv_freq / 2pi) is formed exactly with an FMA two-product of
 // a float head/tail split of inv_freq/2pi (host-computed in double), reduced modulo 1
@@ -42,7 +43,8 @@ __device__ __forceinline__ float rope_turns(int pos, float hi, float lo) {
 // Work item: one token and a chunk of up to RPS * kUnroll of its heads in one part. The
 // chunk's loads (and V loads) are all issued before any arithmetic, so a warp keeps
 // kUnroll 16-byte loads per lane in flight; items are spread over all warps of the grid.
-template <int DH>
+// HAS_V = false drops the optional V copy (and its registers).
+template <int DH, bool HAS_V = true>
 __device__ __forceinline__ void norm_rope_rows(const NormRopeJob& job, int64_t warp_id, int64_t n_warps) {
   constexpr int LR = DH / 8;       // lanes per row
   constexpr int HL = LR / 2;       // lanes per half row
@@ -58,11 +60,13 @@ __device__ __forceinline__ void norm_rope_rows(const NormRopeJob& job, int64_t w
   const int row_in_step = lane / LR;
   const float sgn = half ? 1.0f : -1.0f;
   const float inv_dh = 1.0f / static_cast<float>(DH);
-  float thi[8], tlo[8];
+  static_assert(DH == 64 || DH == 128, "head_dim 64 or 128");
+  constexpr int FPL = DH / 64;  // frequencies computed per lane
+  float thi[FPL], tlo[FPL];
 #pragma unroll
-  for (int e = 0; e < 8; ++e) {
-    thi[e] = job.turns.hi[8 * q + e];
-    tlo[e] = job.turns.lo[8 * q + e];
+  for (int i = 0; i < FPL; ++i) {
+    thi[i] = job.turns.hi[lane * FPL + i];
+    tlo[i] = job.turns.lo[lane * FPL + i];
   }
   const int chunks0 = (job.part[0].heads + HPI - 1) / HPI;
   const int chunks1 = job.nparts > 1 ? (job.part[1].heads + HPI - 1) / HPI : 0;
@@ -93,7 +97,7 @@ __device__ __forceinline__ void norm_rope_rows(const NormRopeJob& job, int64_t w
       vraw[u] = make_uint4(0, 0, 0, 0);
       if (h < P.heads) {
         raw[u] = *reinterpret_cast<const uint4*>(P.src + (t * P.heads + h) * DH + elem0);
-        if (P.v_src) vraw[u] = *reinterpret_cast<const uint4*>(P.v_src + (t * P.heads + h) * DH + elem0);
+        if (HAS_V && P.v_src) vraw[u] = *reinterpret_cast<const uint4*>(P.v_src + (t * P.heads + h) * DH + elem0);
       }
     }
     float w_me[8], w_pa[8];
@@ -110,9 +114,16 @@ __device__ __forceinline__ void norm_rope_rows(const NormRopeJob& job, int64_t w
       }
     }
     const int pos = job.pos[t];
-    float cs[8], sn[8];
+    float mc[FPL], ms[FPL];  // this lane's frequencies lane * FPL + i
 #pragma unroll
-    for (int e = 0; e < 8; ++e) sincospif(2.0f * rope_turns(pos, thi[e], tlo[e]), &sn[e], &cs[e]);
+    for (int i = 0; i < FPL; ++i) sincospif(2.0f * rope_turns(pos, thi[i], tlo[i]), &ms[i], &mc[i]);
+    float cs[8], sn[8];  // frequencies 8q + e, from lane (8q + e) / FPL (8q is a multiple of FPL)
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const int src = (8 * q + e) / FPL;
+      cs[e] = __shfl_sync(0xffffffffu, mc[e % FPL], src);
+      sn[e] = __shfl_sync(0xffffffffu, ms[e % FPL], src);
+    }
 
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
@@ -156,7 +167,7 @@ __device__ __forceinline__ void norm_rope_rows(const NormRopeJob& job, int64_t w
         const int64_t dst_off = (dst_row * P.heads + h) * DH + elem0;
         *reinterpret_cast<uint4*>(P.dst_hi + dst_off) = make_uint4(ohi[0], ohi[1], ohi[2], ohi[3]);
         if (P.dst_lo) *reinterpret_cast<uint4*>(P.dst_lo + dst_off) = make_uint4(olo[0], olo[1], olo[2], olo[3]);
-        if (P.v_src) *reinterpret_cast<uint4*>(P.v_dst + dst_off) = vraw[u];
+        if (HAS_V && P.v_src) *reinterpret_cast<uint4*>(P.v_dst + dst_off) = vraw[u];
       }
     }
   }
