@@ -157,7 +157,7 @@ int dflash_block_attention_plan(int num_reqs, int64_t total_q, int hq, int hkv, 
                                                          max_block_len, window, causal, out_dtype == DFLASH_OUT_F32,
                                                          flags, sms);
   const bool any = num_reqs > 0 && total_q > 0;
-  plan[0] = any ? (w.balanced ? 3 : 2) : 0;
+  plan[0] = any ? ((w.balanced && w.grid > 1) ? 3 : 2) : 0;  // the combine runs only with several CTAs
   plan[1] = static_cast<int64_t>(std::ceil(w.tiles_bound / w.grid));
   plan[2] = w.groups_max;
   plan[3] = any ? w.grid : 0;
