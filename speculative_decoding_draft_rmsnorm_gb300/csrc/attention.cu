@@ -476,6 +476,7 @@ attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
       int iu = 0;
       bool ok = true;
       constexpr uint32_t q_box_bytes_per_row = 128;
+      const uint64_t pol_stream = l2_policy_evict_first();
       SegIter it = make_iter();
       Seg sg;
       for (; ok && it.next(sg); ++iu) {
@@ -494,6 +495,7 @@ attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                         nb * 64, 0, U.kvh, U.qsl + U.tok0);
         }
         const int n = sg.t1 - sg.t0;
+        // context K/V tiles are read once: they should not push the split partials out of L2
         auto issue_k = [&](int t) -> bool {
           const int slot = static_cast<int>(gk % NK);
           if (!mbar_wait(bar(L::K_EMPTY + slot), ((gk / NK) & 1) ^ 1, abort_flag)) return false;
@@ -502,8 +504,12 @@ attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
           const void* map = ti.blk ? static_cast<const void*>(&tm_kb) : static_cast<const void*>(&tm_kc);
 #pragma unroll
           for (int nb = 0; nb < L::NB; ++nb) {
-            tma_load_3d(sbase + L::OFF_K + slot * L::KB + nb * (kTileKeys * 128), map, bar(L::K_FULL + slot), nb * 64,
-                        U.kvh, ti.row);
+            if (ti.blk)
+              tma_load_3d(sbase + L::OFF_K + slot * L::KB + nb * (kTileKeys * 128), map, bar(L::K_FULL + slot),
+                          nb * 64, U.kvh, ti.row);
+            else
+              tma_load_3d_hint(sbase + L::OFF_K + slot * L::KB + nb * (kTileKeys * 128), map, bar(L::K_FULL + slot),
+                               nb * 64, U.kvh, ti.row, pol_stream);
             // precise mode: a block tile holds 64 keys, hi in rows 0-63 and lo in rows 64-127
             if (PRECISE && ti.blk)
               tma_load_3d(sbase + L::OFF_K + slot * L::KB + nb * (kTileKeys * 128) + 64 * 128, &tm_kbl,
@@ -519,9 +525,14 @@ attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
           mbar_arrive_expect_tx(bar(L::V_FULL + slot), L::KB);
           const void* map = ti.blk ? static_cast<const void*>(&tm_vb) : static_cast<const void*>(&tm_vc);
 #pragma unroll
-          for (int nb = 0; nb < L::NB; ++nb)
-            tma_load_3d(sbase + L::OFF_V + slot * L::KB + nb * (kTileKeys * 128), map, bar(L::V_FULL + slot), nb * 64,
-                        U.kvh, ti.row);
+          for (int nb = 0; nb < L::NB; ++nb) {
+            if (ti.blk)
+              tma_load_3d(sbase + L::OFF_V + slot * L::KB + nb * (kTileKeys * 128), map, bar(L::V_FULL + slot),
+                          nb * 64, U.kvh, ti.row);
+            else
+              tma_load_3d_hint(sbase + L::OFF_V + slot * L::KB + nb * (kTileKeys * 128), map, bar(L::V_FULL + slot),
+                               nb * 64, U.kvh, ti.row, pol_stream);
+          }
           ++gv;
           return true;
         };
@@ -826,19 +837,19 @@ attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
               }
           }
         } else {
+          // kept in L2 for the combine pass, which reads them after the streaming
+          const uint64_t pol_keep = l2_policy_evict_last();
           float* dst = p.part_o + (static_cast<int64_t>(sg.slot) * kTileRows + rho) * DH + half * (DH / 2);
 #pragma unroll
           for (int ch = 0; ch < CH; ++ch)
 #pragma unroll
             for (int e = 0; e < 32; e += 4)
-              *reinterpret_cast<float4*>(dst + ch * 32 + e) =
-                  make_float4(__uint_as_float(o[ch][e]), __uint_as_float(o[ch][e + 1]), __uint_as_float(o[ch][e + 2]),
-                              __uint_as_float(o[ch][e + 3]));
-          if (half == 0) {
-            float* ml = p.part_ml + (static_cast<int64_t>(sg.slot) * kTileRows + rho) * 2;
-            ml[0] = m_used;
-            ml[1] = l_tot;
-          }
+              st_global_v4_hint(dst + ch * 32 + e,
+                                make_float4(__uint_as_float(o[ch][e]), __uint_as_float(o[ch][e + 1]),
+                                            __uint_as_float(o[ch][e + 2]), __uint_as_float(o[ch][e + 3])),
+                                pol_keep);
+          if (half == 0)
+            st_global_v2_hint(p.part_ml + (static_cast<int64_t>(sg.slot) * kTileRows + rho) * 2, m_used, l_tot, pol_keep);
         }
       }
       gj += n;
