@@ -254,6 +254,10 @@ def run_gpu(args, b: W.Batch, rank: int, world: int) -> dict | None:
     torch.cuda.synchronize()
     clocks = ClockSampler(dev_index)
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    # untimed GPU work queued first, so that the host is ahead of the GPU when the first timed
+    # step starts (otherwise its launch latency shows up between the events)
+    for _ in range(3):
+        flush.zero_()
     for i in range(args.steps):
         flush.zero_()
         ev[i][0].record(stream)
@@ -292,6 +296,8 @@ def run_gpu(args, b: W.Batch, rank: int, world: int) -> dict | None:
         e2e_step()
     torch.cuda.synchronize()
     eev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+    for _ in range(3):
+        flush.zero_()
     for i in range(args.steps):
         flush.zero_()
         eev[i][0].record(stream)
