@@ -162,10 +162,10 @@ class ClockSampler:
 class Step:
     """Device-resident inputs of one step and the two library calls that make it."""
 
-    def __init__(self, lib, b: W.Batch, flags: int):
+    def __init__(self, lib, b: W.Batch, flags: int, page_size: int = 0):
         import numpy as np
         import torch
-        self.lib, self.b, self.cfg, self.flags = lib, b, b.cfg, flags
+        self.lib, self.b, self.cfg, self.flags, self.page_size = lib, b, b.cfg, flags, page_size
         c = b.cfg
 
         def d16(a):
@@ -182,25 +182,52 @@ class Step:
             end = int(b.ctx_start_loc[r]) + int(b.ctx_lens[r])
             idx.extend(range(end - a, end))
         self.new_idx = np.array(idx, dtype=np.int64)
+        # store row of every context row: itself (contiguous), or its page slot in a pool whose
+        # pages are handed out in a shuffled order (paged)
+        n_ctx = b.ctx_k_raw.shape[0]
+        if page_size:
+            pages_per = [(int(l) + page_size - 1) // page_size for l in b.ctx_lens]
+            n_pages = max(1, sum(pages_per))
+            order = np.random.default_rng(c.seed + 1).permutation(n_pages)
+            self.block_table = np.full((c.num_reqs, max(1, max(pages_per))), -1, dtype=np.int32)
+            store_row = np.zeros(n_ctx, dtype=np.int64)
+            k = 0
+            for r in range(c.num_reqs):
+                for p in range(pages_per[r]):
+                    self.block_table[r, p] = order[k]
+                    k += 1
+                base = int(b.ctx_start_loc[r])
+                j = np.arange(int(b.ctx_lens[r]))
+                store_row[base + j] = self.block_table[r, j // page_size].astype(np.int64) * page_size + j % page_size
+            store_rows = n_pages * page_size
+        else:
+            store_row = np.arange(n_ctx, dtype=np.int64)
+            store_rows = n_ctx
+        self.store_rows = store_rows
         self.host = {
             "k_new": np.ascontiguousarray(b.ctx_k_raw[self.new_idx]),
             "v_new": np.ascontiguousarray(b.ctx_v[self.new_idx]),
             "pos_new": np.ascontiguousarray(b.ctx_pos[self.new_idx]).astype(np.int32),
-            "slot": self.new_idx.astype(np.int32),
+            "slot": store_row[self.new_idx].astype(np.int32),
             "q": b.q, "k_blk": b.k_blk, "v_blk": b.v_blk, "positions": b.positions,
             "qsl": b.query_start_loc, "csl": b.ctx_start_loc, "clen": b.ctx_lens,
         }
+        if page_size:
+            self.host["bt"] = self.block_table
         self.dev = {k: (d16(v) if v.dtype == np.uint16 else d32(v)) for k, v in self.host.items()}
         self.q_norm_w, self.k_norm_w = d16(b.q_norm_w), d16(b.k_norm_w)
-        # the resident context store, built once (untimed)
-        self.ctx_k = torch.empty(b.ctx_k_raw.shape, dtype=torch.bfloat16, device="cuda")
-        self.ctx_v = d16(b.ctx_v)
-        lib.context_kv(d16(b.ctx_k_raw), d32(b.ctx_pos), self.k_norm_w, self.ctx_k, eps=c.eps, theta=c.theta)
+        # the resident context store, built once (untimed): keys normed + rotated into their
+        # store rows by the append kernel itself, values copied there
+        hkv, dh = c.hkv, c.dh
+        self.ctx_k = torch.empty((store_rows, hkv, dh), dtype=torch.bfloat16, device="cuda")
+        self.ctx_v = torch.zeros((store_rows, hkv, dh), dtype=torch.bfloat16, device="cuda")
+        lib.context_kv(d16(b.ctx_k_raw), d32(b.ctx_pos), self.k_norm_w, self.ctx_k, v=d16(b.ctx_v), ctx_v=self.ctx_v,
+                       slot=d32(store_row.astype(np.int32)), eps=c.eps, theta=c.theta)
         self.max_ctx = int(max(1, b.ctx_lens.max(initial=0)))
         self.max_blk = int(max(1, b.block_lens.max(initial=0)))
         t, hq, dh = b.q.shape
         self.out = torch.empty((t, hq, dh), dtype=torch.bfloat16, device="cuda")
-        self.args = (b.cfg.num_reqs, t, hq, c.hkv, dh, b.ctx_k_raw.shape[0], self.max_ctx, self.max_blk, c.causal,
+        self.args = (b.cfg.num_reqs, t, hq, c.hkv, dh, store_rows, self.max_ctx, self.max_blk, c.causal,
                      c.window, lib.OUT_BF16, flags)
         self.plan = lib.plan(*self.args)
         self.ws = lib.alloc_workspace(lib.workspace_size(*self.args))
@@ -215,6 +242,14 @@ class Step:
     def attend(self, dev=None):
         d = dev or self.dev
         c = self.cfg
+        if self.page_size:
+            ps = self.page_size
+            self.lib.block_attention_paged(
+                d["q"], d["k_blk"], d["v_blk"], self.ctx_k.view(-1, ps, c.hkv, c.dh),
+                self.ctx_v.view(-1, ps, c.hkv, c.dh), d["bt"], d["qsl"], d["clen"], d["positions"], self.q_norm_w,
+                self.k_norm_w, max_ctx_len=self.max_ctx, max_block_len=self.max_blk, out=self.out,
+                workspace=self.ws, eps=c.eps, theta=c.theta, causal=c.causal, window=c.window, flags=self.flags)
+            return
         self.lib.block_attention(d["q"], d["k_blk"], d["v_blk"], self.ctx_k, self.ctx_v, d["qsl"], d["csl"],
                                  d["clen"], d["positions"], self.q_norm_w, self.k_norm_w, max_ctx_len=self.max_ctx,
                                  max_block_len=self.max_blk, out=self.out, workspace=self.ws, eps=c.eps,
@@ -234,7 +269,7 @@ def run_gpu(args, b: W.Batch, rank: int, world: int) -> dict | None:
     torch.cuda.set_device(dev_index)
     cfg = b.cfg
     flags = lib.FLAG_FORCE_SPLIT if cfg.force_split else 0
-    st = Step(lib, b, flags)
+    st = Step(lib, b, flags, args.paged)
     counts = algorithmic_counts(cfg, b.ctx_lens, b.block_lens)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
     stream = torch.cuda.current_stream()
@@ -322,7 +357,10 @@ def run_gpu(args, b: W.Batch, rank: int, world: int) -> dict | None:
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic",
-        "config": {**describe(cfg, b.ctx_lens), "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"},
+        "config": {**describe(cfg, b.ctx_lens),
+                   "context": (f"paged: {args.paged}-row pages in shuffled order, block table per request"
+                               if args.paged else "contiguous segments"),
+                   "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"},
         "tflops": world * counts["flops"] * args.steps / (total_ms / 1e3) / 1e12,
         "attention_ms": statistics.mean(attn_ms),
         "append_ms": statistics.mean(s - a for s, a in zip(step_ms, attn_ms)),
@@ -334,7 +372,7 @@ def run_gpu(args, b: W.Batch, rank: int, world: int) -> dict | None:
             "unit": "GB/s",
             "frac": achieved / peaks["hbm_gbs"],
             "peak_source": peak_note,
-            "traffic": recorded_traffic(cfg.name),
+            "traffic": recorded_traffic(cfg.name + (f"_paged{args.paged}" if args.paged else "")),
             "algorithmic_bytes_per_launch": counts["kv_bytes"],
             "tensor_tflops": counts["flops"] / attn_avg_s / 1e12,
             "tensor_frac": counts["flops"] / attn_avg_s / 1e12 / peaks["bf16_tflops"],
@@ -440,6 +478,8 @@ def main() -> int:
     ap.add_argument("--workload", default="qwen3_4b", choices=sorted(W.CONFIGS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--paged", type=int, default=0, choices=[0, 16, 32, 64, 128],
+                    help="context in a page pool of this many rows per page (shuffled page order); 0: contiguous")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

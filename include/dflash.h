@@ -169,6 +169,37 @@ DFLASH_API int dflash_block_attention(const dflash_bf16* q_raw, const dflash_bf1
                            size_t workspace_bytes, int flags, dflash_stream_t stream);
 
 /*
+ * dflash_block_attention_paged -- dflash_block_attention with the context in page pools.
+ * (qwen3_dflash.cpp: the paged path, ForwardPagedBody, reads each layer's context K/V from
+ *  [max_pages, page_size, Hkv, Dh] pools through a per-request block table and the device
+ *  seq_lens, and writes new rows into page slots.)
+ *
+ *   k_pool, v_pool  bf16 [num_pages, page_size, Hkv, Dh]  context keys (normed + rotated,
+ *                   e.g. by dflash_context_kv with slot = page * page_size + offset) and values
+ *   block_table     int32 [num_reqs, max_pages_per_req]   request r's context row j is row
+ *                   j % page_size of page block_table[r * max_pages_per_req + j / page_size]
+ *   num_pages, page_size, max_pages_per_req                page_size in {16, 32, 64, 128};
+ *                   max_ctx_len <= max_pages_per_req * page_size
+ *   ctx_lens        int32 [num_reqs]  live context rows of request r (<= max_pages_per_req *
+ *                   page_size); only the pages that hold them are read
+ * Every other argument is that of dflash_block_attention (there is no ctx_start_loc). The
+ * workspace is sized by dflash_block_attention_workspace_size with total_ctx =
+ * num_pages * page_size. A block-table entry outside [0, num_pages) is recorded in the
+ * device error word (DFLASH_ERR_DEVICE_METADATA through dflash_check_error) and page 0 is
+ * read in its place.
+ */
+DFLASH_API int dflash_block_attention_paged(const dflash_bf16* q_raw, const dflash_bf16* k_blk,
+                                            const dflash_bf16* v_blk, const dflash_bf16* k_pool,
+                                            const dflash_bf16* v_pool, const int32_t* block_table, int64_t num_pages,
+                                            int page_size, int max_pages_per_req, const int32_t* query_start_loc,
+                                            const int32_t* ctx_lens, const int32_t* positions,
+                                            const dflash_bf16* q_norm_w, const dflash_bf16* k_norm_w, int num_reqs,
+                                            int64_t total_q, int hq, int hkv, int dh, int max_ctx_len,
+                                            int max_block_len, float eps, float rope_theta, float scale, int causal,
+                                            int window, int out_dtype, void* out, void* workspace,
+                                            size_t workspace_bytes, int flags, dflash_stream_t stream);
+
+/*
  * dflash_block_attention_noalloc -- dflash_block_attention without a caller workspace.
  * The pages have no counterpart: this entry point exists for callers that cannot
  * allocate device memory themselves (a plugin host that owns every byte of device

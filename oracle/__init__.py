@@ -170,3 +170,31 @@ def block_attention_dense(q, k_blk, v_blk, ctx_k, ctx_v, query_start_loc, ctx_st
     out = np.empty(shape, dtype=np.float64)
     _check(_load().orc_block_attention_dense(*args, _p(out)), "block_attention_dense")
     return out
+
+
+def gather_paged_context(pool, block_table, ctx_lens, page_size: int):
+    """The context rows of every request, gathered from a page pool, and their offsets.
+
+    pool [num_pages, page_size, Hkv, Dh]; block_table [N, max_pages]. Request r's context row j
+    is row j % page_size of page block_table[r, j // page_size] (the paged layout of the
+    DFlash draft's KV store). Returns (rows [sum ctx_lens, Hkv, Dh], ctx_start_loc [N+1]).
+    """
+    pool = np.asarray(pool)
+    bt = np.asarray(block_table, dtype=np.int64)
+    lens = np.asarray(ctx_lens, dtype=np.int64)
+    starts = np.zeros(len(lens) + 1, dtype=np.int32)
+    starts[1:] = np.cumsum(lens)
+    rows = np.empty((int(starts[-1]),) + pool.shape[2:], dtype=pool.dtype)
+    for r, n in enumerate(lens):
+        for j in range(int(n)):
+            rows[starts[r] + j] = pool[bt[r, j // page_size], j % page_size]
+    return rows, starts
+
+
+def block_attention_paged(q, k_blk, v_blk, k_pool, v_pool, block_table, query_start_loc, ctx_lens, positions,
+                          q_norm_w, k_norm_w, page_size: int, **kw) -> np.ndarray:
+    """block_attention with the context read from page pools through a block table."""
+    ck, starts = gather_paged_context(k_pool, block_table, ctx_lens, page_size)
+    cv, _ = gather_paged_context(v_pool, block_table, ctx_lens, page_size)
+    return block_attention(q, k_blk, v_blk, ck, cv, query_start_loc, starts, ctx_lens, positions, q_norm_w,
+                           k_norm_w, **kw)

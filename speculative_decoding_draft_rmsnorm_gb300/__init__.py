@@ -17,7 +17,8 @@ import ctypes
 import os
 import threading
 
-__all__ = ["load", "lib_path", "context_kv", "block_attention", "workspace_size", "plan", "alloc_workspace",
+__all__ = ["load", "lib_path", "context_kv", "block_attention", "block_attention_paged", "workspace_size", "plan",
+           "alloc_workspace",
            "check_error", "DFlashError", "OUT_BF16", "OUT_F32", "FLAG_FORCE_SPLIT", "FLAG_NO_SPLIT",
            "ERR_INVALID_ARG", "ERR_UNSUPPORTED", "ERR_WORKSPACE", "ERR_CUDA", "ERR_DEVICE_TIMEOUT",
            "ERR_DEVICE_METADATA"]
@@ -66,6 +67,10 @@ def load(build_if_missing: bool = True):
         lib.dflash_block_attention.restype = I32
         lib.dflash_block_attention.argtypes = ([P] * 11 + [I32, I64, I32, I32, I32, I64, I32, I32, F32, F32, F32,
                                                            I32, I32, I32, P, P, SZ, I32, P])
+        lib.dflash_block_attention_paged.restype = I32
+        lib.dflash_block_attention_paged.argtypes = ([P] * 6 + [I64, I32, I32] + [P] * 5 +
+                                                     [I32, I64, I32, I32, I32, I32, I32, F32, F32, F32, I32, I32,
+                                                      I32, P, P, SZ, I32, P])
         lib.dflash_block_attention_plan.restype = I32
         lib.dflash_block_attention_plan.argtypes = [I32, I64, I32, I32, I32, I64, I32, I32, I32, I32, I32, I32, P]
         lib.dflash_check_error.restype = I32
@@ -183,6 +188,46 @@ def block_attention(q, k_blk, v_blk, ctx_k, ctx_v, query_start_loc, ctx_start_lo
         _ptr(ctx_lens), _ptr(positions), _ptr(q_norm_w), _ptr(k_norm_w), n, t, hq, hkv, dh, total_ctx,
         int(max_ctx_len), int(max_block_len), float(eps), float(theta), float(scale), int(causal), int(window),
         out_dtype, _ptr(out), _ptr(workspace), workspace.numel(), flags, _stream(stream))
+    _raise(rc)
+    return out
+
+
+def block_attention_paged(q, k_blk, v_blk, k_pool, v_pool, block_table, query_start_loc, ctx_lens, positions,
+                          q_norm_w, k_norm_w, *, max_ctx_len, max_block_len, out=None, workspace=None, eps=1e-6,
+                          theta=1e6, scale=0.0, causal=False, window=0, out_dtype=OUT_BF16, flags=0, stream=None):
+    """block_attention with the context in page pools.
+
+    k_pool / v_pool [num_pages, page_size, Hkv, Dh] bf16; block_table [N, max_pages_per_req] int32
+    (request r's context row j is row j % page_size of page block_table[r, j // page_size]).
+    """
+    import torch
+    t, hq, dh = q.shape
+    hkv = k_blk.shape[1]
+    n = query_start_loc.shape[0] - 1
+    num_pages, page_size = k_pool.shape[0], k_pool.shape[1]
+    max_pages = block_table.shape[1] if block_table.dim() == 2 else 0
+    for name, ten, shp in [("q", q, None), ("k_blk", k_blk, (t, hkv, dh)), ("v_blk", v_blk, (t, hkv, dh)),
+                           ("k_pool", k_pool, (num_pages, page_size, hkv, dh)),
+                           ("v_pool", v_pool, (num_pages, page_size, hkv, dh)),
+                           ("q_norm_w", q_norm_w, (dh,)), ("k_norm_w", k_norm_w, (dh,))]:
+        _check_tensor(name, ten, torch.bfloat16, shp)
+    for name, ten, shp in [("block_table", block_table, (n, max_pages)), ("query_start_loc", query_start_loc, (n + 1,)),
+                           ("ctx_lens", ctx_lens, (n,)), ("positions", positions, (t,))]:
+        _check_tensor(name, ten, torch.int32, shp)
+    odt = torch.float32 if out_dtype == OUT_F32 else torch.bfloat16
+    if out is None:
+        out = torch.empty((t, hq, dh), dtype=odt, device=q.device)
+    _check_tensor("out", out, odt, (t, hq, dh))
+    need = workspace_size(n, t, hq, hkv, dh, num_pages * page_size, max_ctx_len, max_block_len, causal, window,
+                          out_dtype, flags)
+    if workspace is None:
+        workspace = alloc_workspace(need, q.device)
+    _check_tensor("workspace", workspace, torch.uint8)
+    rc = load().dflash_block_attention_paged(
+        _ptr(q), _ptr(k_blk), _ptr(v_blk), _ptr(k_pool), _ptr(v_pool), _ptr(block_table), num_pages, page_size,
+        max_pages, _ptr(query_start_loc), _ptr(ctx_lens), _ptr(positions), _ptr(q_norm_w), _ptr(k_norm_w), n, t, hq,
+        hkv, dh, int(max_ctx_len), int(max_block_len), float(eps), float(theta), float(scale), int(causal),
+        int(window), out_dtype, _ptr(out), _ptr(workspace), workspace.numel(), flags, _stream(stream))
     _raise(rc)
     return out
 

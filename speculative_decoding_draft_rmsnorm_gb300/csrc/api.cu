@@ -165,13 +165,18 @@ int dflash_block_attention_plan(int num_reqs, int64_t total_q, int hq, int hkv, 
   return ok();
 }
 
-int dflash_block_attention(const dflash_bf16* q_raw, const dflash_bf16* k_blk, const dflash_bf16* v_blk,
-                           const dflash_bf16* ctx_k, const dflash_bf16* ctx_v, const int32_t* query_start_loc,
-                           const int32_t* ctx_start_loc, const int32_t* ctx_lens, const int32_t* positions,
-                           const dflash_bf16* q_norm_w, const dflash_bf16* k_norm_w, int num_reqs, int64_t total_q,
-                           int hq, int hkv, int dh, int64_t total_ctx, int max_ctx_len, int max_block_len, float eps,
-                           float rope_theta, float scale, int causal, int window, int out_dtype, void* out,
-                           void* workspace, size_t workspace_bytes, int flags, dflash_stream_t stream) {
+}  // extern "C"
+
+// Both attention entry points: contiguous context segments (block_table == nullptr) or
+// paged pools (ctx_k / ctx_v are the pools, viewed as total_ctx = num_pages * page_size rows).
+static int attention_call(const dflash_bf16* q_raw, const dflash_bf16* k_blk, const dflash_bf16* v_blk,
+                          const dflash_bf16* ctx_k, const dflash_bf16* ctx_v, const int32_t* query_start_loc,
+                          const int32_t* ctx_start_loc, const int32_t* ctx_lens, const int32_t* positions,
+                          const dflash_bf16* q_norm_w, const dflash_bf16* k_norm_w, int num_reqs, int64_t total_q,
+                          int hq, int hkv, int dh, int64_t total_ctx, int max_ctx_len, int max_block_len, float eps,
+                          float rope_theta, float scale, int causal, int window, int out_dtype, void* out,
+                          void* workspace, size_t workspace_bytes, int flags, dflash_stream_t stream, bool paged,
+                          const int32_t* block_table, int max_pages, int page_size) {
   int rc = check_sizes(num_reqs, total_q, hq, hkv, dh, total_ctx, max_ctx_len, max_block_len, out_dtype);
   if (rc != DFLASH_OK) return rc;
   if (causal != 0 && causal != 1) return fail(DFLASH_ERR_INVALID_ARG, "causal must be 0 or 1");
@@ -181,8 +186,8 @@ int dflash_block_attention(const dflash_bf16* q_raw, const dflash_bf16* k_blk, c
     return fail(DFLASH_ERR_INVALID_ARG, "eps must be >= 0, theta > 0 and scale finite");
   if ((flags & ~3) != 0 || flags == 3) return fail(DFLASH_ERR_INVALID_ARG, "unknown or contradictory flags %d", flags);
   if (num_reqs == 0 || total_q == 0) return ok();
-  if (!q_raw || !k_blk || !v_blk || !query_start_loc || !ctx_start_loc || !ctx_lens || !positions || !q_norm_w ||
-      !k_norm_w || !out || !workspace)
+  if (!q_raw || !k_blk || !v_blk || !query_start_loc || (paged ? !block_table : !ctx_start_loc) || !ctx_lens ||
+      !positions || !q_norm_w || !k_norm_w || !out || !workspace)
     return fail(DFLASH_ERR_INVALID_ARG, "null pointer argument");
   if (total_ctx > 0 && (!ctx_k || !ctx_v)) return fail(DFLASH_ERR_INVALID_ARG, "null context K/V with total_ctx > 0");
   if (!aligned16(q_raw) || !aligned16(k_blk) || !aligned16(v_blk) || !aligned16(out) || !aligned16(q_norm_w) ||
@@ -235,6 +240,10 @@ int dflash_block_attention(const dflash_bf16* q_raw, const dflash_bf16* k_blk, c
   h.csl = ctx_start_loc;
   h.clen = ctx_lens;
   h.positions = positions;
+  h.paged = paged;
+  h.block_table = block_table;
+  h.max_pages = max_pages;
+  h.page_size = page_size;
   h.out = out;
   h.ws_hdr = reinterpret_cast<uint32_t*>(ws + w.hdr);
   h.q_hat = reinterpret_cast<uint16_t*>(ws + w.q_hat);
@@ -251,6 +260,44 @@ int dflash_block_attention(const dflash_bf16* q_raw, const dflash_bf16* k_blk, c
   if (e != cudaSuccess)
     return fail(DFLASH_ERR_CUDA, "block attention launch: %s%s%s", cudaGetErrorString(e), msg[0] ? ": " : "", msg);
   return ok();
+}
+
+extern "C" {
+
+int dflash_block_attention(const dflash_bf16* q_raw, const dflash_bf16* k_blk, const dflash_bf16* v_blk,
+                           const dflash_bf16* ctx_k, const dflash_bf16* ctx_v, const int32_t* query_start_loc,
+                           const int32_t* ctx_start_loc, const int32_t* ctx_lens, const int32_t* positions,
+                           const dflash_bf16* q_norm_w, const dflash_bf16* k_norm_w, int num_reqs, int64_t total_q,
+                           int hq, int hkv, int dh, int64_t total_ctx, int max_ctx_len, int max_block_len, float eps,
+                           float rope_theta, float scale, int causal, int window, int out_dtype, void* out,
+                           void* workspace, size_t workspace_bytes, int flags, dflash_stream_t stream) {
+  return attention_call(q_raw, k_blk, v_blk, ctx_k, ctx_v, query_start_loc, ctx_start_loc, ctx_lens, positions,
+                        q_norm_w, k_norm_w, num_reqs, total_q, hq, hkv, dh, total_ctx, max_ctx_len, max_block_len, eps,
+                        rope_theta, scale, causal, window, out_dtype, out, workspace, workspace_bytes, flags, stream,
+                        false, nullptr, 0, 0);
+}
+
+int dflash_block_attention_paged(const dflash_bf16* q_raw, const dflash_bf16* k_blk, const dflash_bf16* v_blk,
+                                 const dflash_bf16* k_pool, const dflash_bf16* v_pool, const int32_t* block_table,
+                                 int64_t num_pages, int page_size, int max_pages_per_req,
+                                 const int32_t* query_start_loc, const int32_t* ctx_lens, const int32_t* positions,
+                                 const dflash_bf16* q_norm_w, const dflash_bf16* k_norm_w, int num_reqs,
+                                 int64_t total_q, int hq, int hkv, int dh, int max_ctx_len, int max_block_len,
+                                 float eps, float rope_theta, float scale, int causal, int window, int out_dtype,
+                                 void* out, void* workspace, size_t workspace_bytes, int flags,
+                                 dflash_stream_t stream) {
+  if (page_size != 16 && page_size != 32 && page_size != 64 && page_size != 128)
+    return fail(DFLASH_ERR_UNSUPPORTED, "page_size %d: only 16, 32, 64 and 128 are implemented", page_size);
+  if (num_pages < 0 || max_pages_per_req < 0) return fail(DFLASH_ERR_INVALID_ARG, "negative page count");
+  if (num_pages > (0x7fffffffLL - 256) / page_size)
+    return fail(DFLASH_ERR_UNSUPPORTED, "the pools must hold fewer than 2^31 rows (num_pages=%lld)",
+                static_cast<long long>(num_pages));
+  if (static_cast<int64_t>(max_pages_per_req) * page_size < max_ctx_len)
+    return fail(DFLASH_ERR_INVALID_ARG, "max_ctx_len %d exceeds max_pages_per_req x page_size", max_ctx_len);
+  return attention_call(q_raw, k_blk, v_blk, k_pool, v_pool, query_start_loc, nullptr, ctx_lens, positions, q_norm_w,
+                        k_norm_w, num_reqs, total_q, hq, hkv, dh, num_pages * page_size, max_ctx_len, max_block_len,
+                        eps, rope_theta, scale, causal, window, out_dtype, out, workspace, workspace_bytes, flags,
+                        stream, true, block_table, max_pages_per_req, page_size);
 }
 
 int dflash_check_error(const void* workspace, dflash_stream_t stream) {

@@ -53,6 +53,8 @@ struct PrologueParams {
   int num_reqs, hkv, g, tpq, causal, window;
   int groups_max, max_ctx_len, max_block_len;
   int blk_tile;  // keys per block-key tile: 128, or 64 when hi and lo halves share a tile
+  int paged;     // paged context: no ctx_start_loc; capacity paged_cap rows per request
+  int page_size, paged_cap;
 };
 
 __device__ __forceinline__ void load_group(const Group* groups, int g, Group& G) {
@@ -128,8 +130,8 @@ __device__ void build_groups(const PrologueParams& p) {
       // all loads of the request are independent: one round trip
       q.q0 = p.qsl[q.r];
       const int q1 = p.qsl[q.r + 1];
-      q.c0 = p.csl[q.r];
-      const int c1 = p.csl[q.r + 1];
+      q.c0 = p.paged ? 0 : p.csl[q.r];
+      const int c1 = p.paged ? p.paged_cap : p.csl[q.r + 1];
       q.C = p.clen[q.r];
       q.B = q1 - q.q0;
       if ((q.r == 0 && q.q0 != 0) || (q.r == p.num_reqs - 1 && q1 != p.total_q)) s_bad_global = 1;
@@ -141,6 +143,8 @@ __device__ void build_groups(const PrologueParams& p) {
       }
       if (q.B > 0) {
         q.lo = (p.causal && p.window > 0) ? max(0, q.C - p.window + 1) : 0;
+        // paged: context tiles start on a page boundary (keys before the window are masked)
+        if (p.paged) q.lo -= q.lo % p.page_size;
         q.nct = (q.C - q.lo + kTileKeys - 1) / kTileKeys;
         q.n = q.nct + (q.B + p.blk_tile - 1) / p.blk_tile;
         q.QT = (q.B + p.tpq - 1) / p.tpq;
@@ -305,6 +309,11 @@ struct Layout {
 
 struct AttnParams {
   const Group* groups;
+  // paged context (null: contiguous): request r's context key j is pool row
+  // block_table[r * max_pages + j / page_size] * page_size + j % page_size
+  const int32_t* block_table;
+  int max_pages, page_size;
+  int64_t num_pages;
   const CtaRecord* cta_rec;  // balanced schedule
   uint32_t* hdr;
   float* part_o;
@@ -386,7 +395,7 @@ struct SegIter {
   }
 };
 
-template <int DH, int NK, int NV, int NQ, bool PRECISE>
+template <int DH, int NK, int NV, int NQ, bool PRECISE, bool PAGED>
 __global__ void __launch_bounds__(192, 1)
 attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_kc,
                  const __grid_constant__ CUtensorMap tm_vc, const __grid_constant__ CUtensorMap tm_kb,
@@ -536,6 +545,72 @@ attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
           ++gv;
           return true;
         };
+        if constexpr (PAGED) {
+          // Paged context: a context tile is the boxes of the pages holding its keys
+          // [j0, j0 + valid), each page_size rows at its rows of the tile; expect_tx counts only
+          // those (the MMA and the softmax never read rows past valid rounded up to 16, and the
+          // softmax zeroes V rows in that gap). The page indices of tile t + 2 are loaded while
+          // tiles t and t + 1 are issued, so the producer does not wait for them.
+          constexpr int kMaxSub = kTileKeys / 16;
+          const int ps = p.page_size;
+          const int32_t* bt_row = p.block_table + static_cast<int64_t>(U.r) * p.max_pages;
+          auto load_pages = [&](int (&pg)[kMaxSub], int t) {
+            int nsub = 0, first = 0;
+            if (t < sg.t1) {
+              const TileInfo ti = tile_info(U, t, p.blk_tile);
+              if (!ti.blk) {
+                nsub = (ti.valid + ps - 1) / ps;
+                first = ti.j0 / ps;
+              }
+            }
+#pragma unroll
+            for (int s = 0; s < kMaxSub; ++s) pg[s] = s < nsub ? __ldg(bt_row + first + s) : 0;
+          };
+          auto issue_paged = [&](const int (&pg)[kMaxSub], int t, bool is_k) -> bool {
+            const TileInfo ti = tile_info(U, t, p.blk_tile);
+            if (ti.blk) return is_k ? issue_k(t) : issue_v(t);
+            const uint32_t cnt = is_k ? gk : gv;
+            const int nst = is_k ? NK : NV;
+            const int slot = static_cast<int>(cnt % nst);
+            const uint32_t full = bar((is_k ? L::K_FULL : L::V_FULL) + slot);
+            if (!mbar_wait(bar((is_k ? L::K_EMPTY : L::V_EMPTY) + slot), ((cnt / nst) & 1) ^ 1, abort_flag))
+              return false;
+            const int nsub = (ti.valid + ps - 1) / ps;
+            mbar_arrive_expect_tx(full, static_cast<uint32_t>(nsub * ps * 128 * L::NB));
+            const uint32_t dst = sbase + (is_k ? L::OFF_K : L::OFF_V) + slot * L::KB;
+            const void* map = is_k ? static_cast<const void*>(&tm_kc) : static_cast<const void*>(&tm_vc);
+#pragma unroll
+            for (int s = 0; s < kMaxSub; ++s) {
+              if (s >= nsub) break;
+              int pg_s = pg[s];
+              if (pg_s < 0 || pg_s >= p.num_pages) {  // reported; page 0 keeps the copy in bounds
+                atomicOr(&p.hdr[0], kErrMetadata);
+                pg_s = 0;
+              }
+#pragma unroll
+              for (int nb = 0; nb < L::NB; ++nb)
+                tma_load_3d_hint(dst + nb * (kTileKeys * 128) + s * ps * 128, map, full, nb * 64, U.kvh, pg_s * ps,
+                                 pol_stream);
+            }
+            if (is_k) ++gk; else ++gv;
+            return true;
+          };
+          int pa[kMaxSub], pb[kMaxSub], pc[kMaxSub];
+          load_pages(pa, sg.t0);
+          load_pages(pb, sg.t0 + 1);
+          if (!(ok = issue_paged(pa, sg.t0, true))) break;
+          for (int j = 0; j < n && ok; ++j) {
+            load_pages(pc, sg.t0 + j + 2);
+            if (j + 1 < n) ok = issue_paged(pb, sg.t0 + j + 1, true);
+            if (ok) ok = issue_paged(pa, sg.t0 + j, false);
+#pragma unroll
+            for (int s = 0; s < kMaxSub; ++s) {
+              pa[s] = pb[s];
+              pb[s] = pc[s];
+            }
+          }
+          continue;
+        }
         if (!(ok = issue_k(sg.t0))) break;
         for (int j = 0; j < n && ok; ++j) {
           if (j + 1 < n) ok = issue_k(sg.t0 + j + 1);
@@ -1062,13 +1137,13 @@ WorkspacePlan plan_workspace(int num_reqs, int64_t total_q, int hq, int hkv, int
   return w;
 }
 
-template <int DH, int NK, int NV, int NQ, bool PRECISE>
+template <int DH, int NK, int NV, int NQ, bool PRECISE, bool PAGED>
 static cudaError_t launch_b(const CUtensorMap& tq, const CUtensorMap& tkc, const CUtensorMap& tvc,
                             const CUtensorMap& tkb, const CUtensorMap& tvb, const CUtensorMap& tql,
                             const CUtensorMap& tkbl, const AttnParams& ap, int grid, cudaStream_t stream) {
   using L = Layout<DH, NK, NV, NQ, PRECISE>;
   static_assert(L::ALLOC <= 232448, "shared memory plan exceeds the per-block limit");
-  auto kern = attention_kernel<DH, NK, NV, NQ, PRECISE>;
+  auto kern = attention_kernel<DH, NK, NV, NQ, PRECISE, PAGED>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg{};
@@ -1132,6 +1207,9 @@ cudaError_t launch_attention(const AttnHost& h, cudaStream_t stream, char* msg, 
   pp.max_ctx_len = h.max_ctx_len;
   pp.max_block_len = h.max_block_len;
   pp.blk_tile = h.precise ? 64 : kTileKeys;
+  pp.paged = h.paged ? 1 : 0;
+  pp.page_size = h.paged ? h.page_size : 1;
+  pp.paged_cap = h.paged ? h.max_pages * h.page_size : 0;
   cudaError_t e = cudaSuccess;
   int64_t nr_blocks = (h.total_q * norm_rope_items_per_token(pp.job, h.dh) + 7) / 8;
   nr_blocks = std::min<int64_t>(nr_blocks, static_cast<int64_t>(h.num_sms) * 3 - 1);  // all co-resident
@@ -1148,8 +1226,8 @@ cudaError_t launch_attention(const AttnHost& h, cudaStream_t stream, char* msg, 
   const void* ctx_v = h.total_ctx > 0 ? static_cast<const void*>(h.ctx_v) : static_cast<const void*>(h.q_hat);
   const int64_t ctx_rows = h.total_ctx > 0 ? h.total_ctx : 1;
   bool ok = encode_q_map(&tq, h.q_hat, h.dh, h.g, h.hkv, h.total_q, h.tpq) &&
-            encode_rows_map(&tkc, ctx_k, h.dh, h.hkv, ctx_rows, kTileKeys) &&
-            encode_rows_map(&tvc, ctx_v, h.dh, h.hkv, ctx_rows, kTileKeys) &&
+            encode_rows_map(&tkc, ctx_k, h.dh, h.hkv, ctx_rows, h.paged ? h.page_size : kTileKeys) &&
+            encode_rows_map(&tvc, ctx_v, h.dh, h.hkv, ctx_rows, h.paged ? h.page_size : kTileKeys) &&
             encode_rows_map(&tkb, h.k_hat, h.dh, h.hkv, h.total_q, h.precise ? 64 : kTileKeys) &&
             encode_rows_map(&tvb, h.v_blk, h.dh, h.hkv, h.total_q, kTileKeys);
   if (ok && h.precise)
@@ -1177,22 +1255,32 @@ cudaError_t launch_attention(const AttnHost& h, cudaStream_t stream, char* msg, 
   ap.window = h.window;
   ap.scale_log2 = h.scale_log2;
   ap.blk_tile = h.precise ? 64 : kTileKeys;
+  ap.block_table = h.paged ? h.block_table : nullptr;
+  ap.max_pages = h.max_pages;
+  ap.page_size = h.paged ? h.page_size : kTileKeys;
+  ap.num_pages = h.paged ? h.total_ctx / h.page_size : 0;
   ap.balanced = h.balanced ? 1 : 0;
   ap.grid = h.grid;
   const int grid_b = h.grid;
   // ---- B: attention
-  // K/V ring split for Dh = 128 (five 32 KB stages): DFLASH_RING=23 selects 2 K + 3 V stages
-  static const bool ring23 = [] {
-    const char* e = std::getenv("DFLASH_RING");
-    return e != nullptr && std::strcmp(e, "23") == 0;
-  }();
-  if (h.dh == 128)
-    e = h.precise ? launch_b<128, 2, 2, 1, true>(tq, tkc, tvc, tkb, tvb, tql, tkbl, ap, grid_b, stream)
-        : ring23  ? launch_b<128, 2, 3, 2, false>(tq, tkc, tvc, tkb, tvb, tql, tkbl, ap, grid_b, stream)
-                  : launch_b<128, 3, 2, 2, false>(tq, tkc, tvc, tkb, tvb, tql, tkbl, ap, grid_b, stream);
-  else
-    e = h.precise ? launch_b<64, 3, 3, 2, true>(tq, tkc, tvc, tkb, tvb, tql, tkbl, ap, grid_b, stream)
-                  : launch_b<64, 4, 4, 2, false>(tq, tkc, tvc, tkb, tvb, tql, tkbl, ap, grid_b, stream);
+  // K/V rings: Dh = 128, 3 K + 2 V stages of 32 KB (2 + 2 with the hi/lo halves of precise
+  // mode); Dh = 64, 4 + 4 (3 + 3). Paged contexts have their own instantiations, so that the
+  // contiguous kernels carry no paged code.
+  if (h.paged) {
+    if (h.dh == 128)
+      e = h.precise ? launch_b<128, 2, 2, 1, true, true>(tq, tkc, tvc, tkb, tvb, tql, tkbl, ap, grid_b, stream)
+                    : launch_b<128, 3, 2, 2, false, true>(tq, tkc, tvc, tkb, tvb, tql, tkbl, ap, grid_b, stream);
+    else
+      e = h.precise ? launch_b<64, 3, 3, 2, true, true>(tq, tkc, tvc, tkb, tvb, tql, tkbl, ap, grid_b, stream)
+                    : launch_b<64, 4, 4, 2, false, true>(tq, tkc, tvc, tkb, tvb, tql, tkbl, ap, grid_b, stream);
+  } else {
+    if (h.dh == 128)
+      e = h.precise ? launch_b<128, 2, 2, 1, true, false>(tq, tkc, tvc, tkb, tvb, tql, tkbl, ap, grid_b, stream)
+                    : launch_b<128, 3, 2, 2, false, false>(tq, tkc, tvc, tkb, tvb, tql, tkbl, ap, grid_b, stream);
+    else
+      e = h.precise ? launch_b<64, 3, 3, 2, true, false>(tq, tkc, tvc, tkb, tvb, tql, tkbl, ap, grid_b, stream)
+                    : launch_b<64, 4, 4, 2, false, false>(tq, tkc, tvc, tkb, tvb, tql, tkbl, ap, grid_b, stream);
+  }
   if (e != cudaSuccess) return e;
   // ---- C: combine split partials
   if (h.balanced && h.grid > 1) {  // one block per CTA boundary and 16-row slice

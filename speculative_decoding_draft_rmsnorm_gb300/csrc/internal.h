@@ -88,7 +88,12 @@ struct AttnHost {
   int num_sms;
   // device pointers
   const uint16_t *q, *k_blk, *v_blk, *ctx_k, *ctx_v, *q_norm_w, *k_norm_w;
-  const int32_t *qsl, *csl, *clen, *positions;
+  const int32_t *qsl, *csl, *clen, *positions;  // csl: contiguous context only
+  // paged context: ctx_k / ctx_v are pools of page_size-row pages; request r's context row j
+  // is pool row block_table[r * max_pages + j / page_size] * page_size + j % page_size
+  bool paged;
+  const int32_t* block_table;
+  int max_pages, page_size;
   void* out;
   // workspace carve-up
   uint32_t* ws_hdr;   // [0] error word, [1] group count, [2] total key tiles

@@ -72,3 +72,25 @@ def assert_close_f32(got: np.ndarray, want: np.ndarray, what: str = "") -> None:
     d = np.abs(got - want)
     assert np.all(np.isfinite(got)), f"{what}: non-finite output"
     assert d.max() <= F32_MAX_ABS, f"{what}: max|diff| {d.max():.3e} > {F32_MAX_ABS}"
+
+
+def to_pages(rows: np.ndarray, starts: np.ndarray, lens: np.ndarray, page_size: int, order, fill=np.uint16(0)):
+    """Lays request r's first lens[r] rows (rows[starts[r]:]) into pages of a pool; the k-th page
+    allocated (in request order) is pool page order[k]. Returns (pool, block_table) with unused
+    block-table entries -1."""
+    n = len(lens)
+    pages_per = [(int(l) + page_size - 1) // page_size for l in lens]
+    total = max(1, sum(pages_per))
+    max_pages = max(1, max(pages_per, default=1))
+    pool = np.full((total, page_size) + rows.shape[1:], fill, dtype=rows.dtype)
+    bt = np.full((n, max_pages), -1, dtype=np.int32)
+    k = 0
+    for r in range(n):
+        for p in range(pages_per[r]):
+            page = int(order[k])
+            k += 1
+            bt[r, p] = page
+            lo = p * page_size
+            hi = min(int(lens[r]), lo + page_size)
+            pool[page, : hi - lo] = rows[starts[r] + lo: starts[r] + hi]
+    return pool, bt
