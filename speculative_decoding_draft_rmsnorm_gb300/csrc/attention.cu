@@ -395,6 +395,123 @@ struct SegIter {
   }
 };
 
+// Producer of the paged instantiation (the whole warp 0). Q and block tiles come by TMA from
+// lane 0. A context tile is one TMA box of page_size rows per page that holds its live keys,
+// each at its rows of the tile: lane 0 posts the tile's byte count on the barrier and lane s
+// issues the box of the tile's s-th page, so the boxes of a tile go out in parallel. Rows
+// past the last such page are not loaded (the MMA and the softmax never read past the
+// valid keys rounded up to 16, and the softmax zeroes the V rows in that gap). Page indices
+// are loaded two tiles ahead.
+template <int DH, int NK, int NV, int NQ, bool PRECISE>
+__device__ __forceinline__ void produce_paged(const AttnParams& p, const CUtensorMap* tm_q, const CUtensorMap* tm_ql,
+                                              const CUtensorMap* tm_kc, const CUtensorMap* tm_vc,
+                                              const CUtensorMap* tm_kb, const CUtensorMap* tm_vb,
+                                              const CUtensorMap* tm_kbl, SegIter it, uint32_t sbase, uint32_t bar0,
+                                              volatile int* abort_flag, int lane) {
+  const uint64_t pol_stream = l2_policy_evict_first();
+  using L = Layout<DH, NK, NV, NQ, PRECISE>;
+  auto bar = [&](int i) -> uint32_t { return bar0 + 8u * static_cast<uint32_t>(i); };
+  auto wait0 = [&](uint32_t b, uint32_t parity) -> bool {  // lane 0 waits; every lane learns the outcome
+    int r = 1;
+    if (lane == 0) r = mbar_wait(b, parity, abort_flag) ? 1 : 0;
+    return __shfl_sync(0xffffffffu, r, 0) != 0;
+  };
+  const int ps = p.page_size;
+  uint32_t gk = 0, gv = 0;
+  int iu = 0;
+  bool ok = true;
+  Seg sg;
+  for (; ok && it.next(sg); ++iu) {
+    const Group& U = sg.grp;
+    const int qb = iu % NQ;
+    if (!(ok = wait0(bar(L::Q_EMPTY + qb), ((iu / NQ) & 1) ^ 1))) break;
+    if (lane == 0) {
+      const uint32_t q_rows = static_cast<uint32_t>(p.g * (kTileRows / p.g));
+      mbar_arrive_expect_tx(bar(L::Q_FULL + qb), (PRECISE ? 2 : 1) * L::NB * q_rows * 128);
+#pragma unroll
+      for (int nb = 0; nb < L::NB; ++nb) {
+        tma_load_4d(sbase + L::OFF_Q + qb * L::QBT + nb * (kTileRows * 128), tm_q, bar(L::Q_FULL + qb), nb * 64, 0,
+                    U.kvh, U.qsl + U.tok0);
+        if (PRECISE)
+          tma_load_4d(sbase + L::OFF_Q + qb * L::QBT + L::QB + nb * (kTileRows * 128), tm_ql, bar(L::Q_FULL + qb),
+                      nb * 64, 0, U.kvh, U.qsl + U.tok0);
+      }
+    }
+    const int n = sg.t1 - sg.t0;
+    const int32_t* bt_row = p.block_table + static_cast<int64_t>(U.r) * p.max_pages;
+    // lane s holds the index of the tile's s-th page
+    auto tile_page = [&](int t) -> int {
+      if (t >= sg.t1) return 0;
+      const TileInfo ti = tile_info(U, t, p.blk_tile);
+      if (ti.blk) return 0;
+      const int nsub = (ti.valid + ps - 1) / ps;
+      return lane < nsub ? __ldg(bt_row + ti.j0 / ps + lane) : 0;
+    };
+    auto issue = [&](int t, bool is_k, int pg) -> bool {
+      const uint32_t cnt = is_k ? gk : gv;
+      const int nst = is_k ? NK : NV;
+      const int slot = static_cast<int>(cnt % nst);
+      const uint32_t full = bar((is_k ? L::K_FULL : L::V_FULL) + slot);
+      if (!wait0(bar((is_k ? L::K_EMPTY : L::V_EMPTY) + slot), ((cnt / nst) & 1) ^ 1)) return false;
+      const TileInfo ti = tile_info(U, t, p.blk_tile);
+      const uint32_t dst = sbase + (is_k ? L::OFF_K : L::OFF_V) + slot * L::KB;
+      if (ti.blk) {
+        if (lane == 0) {
+          mbar_arrive_expect_tx(full, L::KB);
+#pragma unroll
+          for (int nb = 0; nb < L::NB; ++nb) {
+            tma_load_3d(dst + nb * (kTileKeys * 128), is_k ? tm_kb : tm_vb, full, nb * 64, U.kvh, ti.row);
+            if (PRECISE && is_k)  // a block tile holds 64 keys, hi in rows 0-63 and lo in rows 64-127
+              tma_load_3d(dst + nb * (kTileKeys * 128) + 64 * 128, tm_kbl, full, nb * 64, U.kvh, ti.row);
+          }
+        }
+      } else {
+        const int nsub = (ti.valid + ps - 1) / ps;
+        if (lane == 0) mbar_arrive_expect_tx(full, static_cast<uint32_t>(nsub * ps * 128 * L::NB));
+        if (lane < nsub && (pg < 0 || pg >= p.num_pages)) {  // reported; page 0 keeps the copy in bounds
+          atomicOr(&p.hdr[0], kErrMetadata);
+          pg = 0;
+        }
+        // one box per lane: lane b copies 64-column half b % NB of page b / NB
+        const int my_page = __shfl_sync(0xffffffffu, pg, (lane / L::NB) & 31);
+        if (lane < nsub * L::NB) {
+          const int sp = lane / L::NB, nb = lane % L::NB;
+          const void* map = is_k ? static_cast<const void*>(tm_kc) : static_cast<const void*>(tm_vc);
+          tma_load_3d_hint(dst + nb * (kTileKeys * 128) + sp * ps * 128, map, full, nb * 64, U.kvh, my_page * ps,
+                           pol_stream);
+        }
+      }
+      if (is_k) ++gk; else ++gv;
+      return true;
+    };
+    int pa = tile_page(sg.t0), pb = tile_page(sg.t0 + 1);
+    if (!(ok = issue(sg.t0, true, pa))) break;
+    for (int j = 0; j < n && ok; ++j) {
+      const int pc = tile_page(sg.t0 + j + 2);
+      if (j + 1 < n) ok = issue(sg.t0 + j + 1, true, pb);
+      if (ok) ok = issue(sg.t0 + j, false, pa);
+      pa = pb;
+      pb = pc;
+    }
+  }
+  if (!ok && lane == 0) atomicOr(&p.hdr[0], kErrTimeout);
+  // every copy into shared memory has landed before the CTA can exit
+  if (lane == 0) {
+    for (int s = 0; s < NK; ++s)
+      if (gk > static_cast<uint32_t>(s)) {
+        const uint32_t last = ((gk - 1 - s) / NK) * NK + s;
+        int dummy = 0;
+        mbar_wait(bar(L::K_FULL + s), (last / NK) & 1, &dummy);
+      }
+    for (int s = 0; s < NV; ++s)
+      if (gv > static_cast<uint32_t>(s)) {
+        const uint32_t last = ((gv - 1 - s) / NV) * NV + s;
+        int dummy = 0;
+        mbar_wait(bar(L::V_FULL + s), (last / NV) & 1, &dummy);
+      }
+  }
+}
+
 template <int DH, int NK, int NV, int NQ, bool PRECISE, bool PAGED>
 __global__ void __launch_bounds__(192, 1)
 attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_kc,
@@ -480,7 +597,10 @@ attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
-    if (lane == 0) {
+    if constexpr (PAGED) {
+      produce_paged<DH, NK, NV, NQ, PRECISE>(p, &tm_q, &tm_ql, &tm_kc, &tm_vc, &tm_kb, &tm_vb, &tm_kbl, make_iter(),
+                                             sbase, bar0, abort_flag, lane);
+    } else if (lane == 0) {
       uint32_t gk = 0, gv = 0;
       int iu = 0;
       bool ok = true;
@@ -545,72 +665,6 @@ attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
           ++gv;
           return true;
         };
-        if constexpr (PAGED) {
-          // Paged context: a context tile is the boxes of the pages holding its keys
-          // [j0, j0 + valid), each page_size rows at its rows of the tile; expect_tx counts only
-          // those (the MMA and the softmax never read rows past valid rounded up to 16, and the
-          // softmax zeroes V rows in that gap). The page indices of tile t + 2 are loaded while
-          // tiles t and t + 1 are issued, so the producer does not wait for them.
-          constexpr int kMaxSub = kTileKeys / 16;
-          const int ps = p.page_size;
-          const int32_t* bt_row = p.block_table + static_cast<int64_t>(U.r) * p.max_pages;
-          auto load_pages = [&](int (&pg)[kMaxSub], int t) {
-            int nsub = 0, first = 0;
-            if (t < sg.t1) {
-              const TileInfo ti = tile_info(U, t, p.blk_tile);
-              if (!ti.blk) {
-                nsub = (ti.valid + ps - 1) / ps;
-                first = ti.j0 / ps;
-              }
-            }
-#pragma unroll
-            for (int s = 0; s < kMaxSub; ++s) pg[s] = s < nsub ? __ldg(bt_row + first + s) : 0;
-          };
-          auto issue_paged = [&](const int (&pg)[kMaxSub], int t, bool is_k) -> bool {
-            const TileInfo ti = tile_info(U, t, p.blk_tile);
-            if (ti.blk) return is_k ? issue_k(t) : issue_v(t);
-            const uint32_t cnt = is_k ? gk : gv;
-            const int nst = is_k ? NK : NV;
-            const int slot = static_cast<int>(cnt % nst);
-            const uint32_t full = bar((is_k ? L::K_FULL : L::V_FULL) + slot);
-            if (!mbar_wait(bar((is_k ? L::K_EMPTY : L::V_EMPTY) + slot), ((cnt / nst) & 1) ^ 1, abort_flag))
-              return false;
-            const int nsub = (ti.valid + ps - 1) / ps;
-            mbar_arrive_expect_tx(full, static_cast<uint32_t>(nsub * ps * 128 * L::NB));
-            const uint32_t dst = sbase + (is_k ? L::OFF_K : L::OFF_V) + slot * L::KB;
-            const void* map = is_k ? static_cast<const void*>(&tm_kc) : static_cast<const void*>(&tm_vc);
-#pragma unroll
-            for (int s = 0; s < kMaxSub; ++s) {
-              if (s >= nsub) break;
-              int pg_s = pg[s];
-              if (pg_s < 0 || pg_s >= p.num_pages) {  // reported; page 0 keeps the copy in bounds
-                atomicOr(&p.hdr[0], kErrMetadata);
-                pg_s = 0;
-              }
-#pragma unroll
-              for (int nb = 0; nb < L::NB; ++nb)
-                tma_load_3d_hint(dst + nb * (kTileKeys * 128) + s * ps * 128, map, full, nb * 64, U.kvh, pg_s * ps,
-                                 pol_stream);
-            }
-            if (is_k) ++gk; else ++gv;
-            return true;
-          };
-          int pa[kMaxSub], pb[kMaxSub], pc[kMaxSub];
-          load_pages(pa, sg.t0);
-          load_pages(pb, sg.t0 + 1);
-          if (!(ok = issue_paged(pa, sg.t0, true))) break;
-          for (int j = 0; j < n && ok; ++j) {
-            load_pages(pc, sg.t0 + j + 2);
-            if (j + 1 < n) ok = issue_paged(pb, sg.t0 + j + 1, true);
-            if (ok) ok = issue_paged(pa, sg.t0 + j, false);
-#pragma unroll
-            for (int s = 0; s < kMaxSub; ++s) {
-              pa[s] = pb[s];
-              pb[s] = pc[s];
-            }
-          }
-          continue;
-        }
         if (!(ok = issue_k(sg.t0))) break;
         for (int j = 0; j < n && ok; ++j) {
           if (j + 1 < n) ok = issue_k(sg.t0 + j + 1);
