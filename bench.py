@@ -90,10 +90,14 @@ def load_peaks() -> tuple[dict, str]:
         return {"hbm_gbs": FALLBACK_HBM_GBS, "bf16_tflops": FALLBACK_BF16_TFLOPS}, "of fallback"
 
 
+# the sources of the three launches of one attention call (prologue, attention, combine)
+ATTENTION_SOURCES = ("api.cu", "attention.cu", "internal.h", "norm_rope.cuh", "ptx.cuh")
+
+
 def kernel_source_hash() -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "speculative_decoding_draft_rmsnorm_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
+    for name in ATTENTION_SOURCES:
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode() + f.read())
     return h.hexdigest()[:16]
