@@ -198,3 +198,62 @@ def block_attention_paged(q, k_blk, v_blk, k_pool, v_pool, block_table, query_st
     cv, _ = gather_paged_context(v_pool, block_table, ctx_lens, page_size)
     return block_attention(q, k_blk, v_blk, ck, cv, query_start_loc, starts, ctx_lens, positions, q_norm_w,
                            k_norm_w, **kw)
+
+
+def paged_append(k_pool, v_pool, block_table, seq_lens, new_start_loc, k_raw, v, k_norm_w, page_size: int,
+                 eps: float = 1e-6, theta: float = 1e6):
+    """Appends every request's new context rows to its pages and advances its length.
+
+    qwen3_dflash.cpp, AppendContextKVDevice (the paged draft KV store): the new rows of a
+    request sit at the positions that follow its stored context, [L, L + count) with L its
+    current length; each is projected as PrecomputeContextKVDevice does (k_norm, then NeoX
+    RoPE at that position, stored in bf16; V raw) and lands at row p % page_size of page
+    block_table[r, p // page_size]; the length then grows by count.
+
+    Rows new_start_loc[r] .. new_start_loc[r+1] of k_raw / v belong to request r; rows
+    outside [new_start_loc[0], new_start_loc[N]) belong to none and are ignored. A row whose
+    page index is past the table, or whose page id is outside the pool, is not written and
+    sets the returned flag. new_start_loc must be nondecreasing, start at >= 0 and end at
+    <= len(k_raw); otherwise nothing changes and the flag is set.
+
+    Returns (k_pool, v_pool, seq_lens, flag): new arrays, the inputs are not modified.
+    """
+    kp = np.array(k_pool, dtype=np.uint16, copy=True)
+    vp = np.array(v_pool, dtype=np.uint16, copy=True)
+    lens = np.array(seq_lens, dtype=np.int64, copy=True)
+    nsl = np.asarray(new_start_loc, dtype=np.int64)
+    bt = np.asarray(block_table, dtype=np.int64)
+    k_raw = _u16(k_raw)
+    v = _u16(v)
+    n = k_raw.shape[0]
+    n_req = len(nsl) - 1
+    num_pages, max_pages = kp.shape[0], bt.shape[1]
+    if nsl[0] < 0 or nsl[n_req] > n or np.any(np.diff(nsl) < 0):
+        return kp, vp, lens.astype(np.int32), True
+    flag = False
+    rows, dst_page, dst_off, pos = [], [], [], []
+    for r in range(n_req):
+        for i in range(int(nsl[r + 1] - nsl[r])):
+            p = int(lens[r]) + i
+            if p < 0 or p // page_size >= max_pages:
+                flag = True
+                continue
+            page = int(bt[r, p // page_size])
+            if page < 0 or page >= num_pages:
+                flag = True
+                continue
+            rows.append(int(nsl[r]) + i)
+            dst_page.append(page)
+            dst_off.append(p % page_size)
+            pos.append(p)
+    if rows:
+        k16 = context_kv(k_raw[rows], np.array(pos, dtype=np.int32), k_norm_w, eps, theta)[1]
+        for j, (pg, off) in enumerate(zip(dst_page, dst_off)):
+            kp[pg, off] = k16[j]
+            if v is not None:
+                vp[pg, off] = v[rows[j]]
+    lens += np.diff(nsl)
+    return kp, vp, lens.astype(np.int32), flag
+
+
+from .prepare_inputs import prepare_dflash_inputs  # noqa: E402  (pure integer, no C part)

@@ -218,3 +218,83 @@ def make_batch(cfg: Config, ctx_lens=None, block_lens=None, seed: int | None = N
         q_norm_w=uniform_bf16(s, STREAM_QW, cfg.dh, 0.5, 1.5),
         k_norm_w=uniform_bf16(s, STREAM_KW, cfg.dh, 0.5, 1.5),
     )
+
+
+# ---------------------------------------------------------------- draft-step input preparation
+STREAM_PREP = 8
+
+
+@dataclass
+class PrepareBatch:
+    """Integer inputs of one draft step's input preparation (vllm.cpp qwen3_dflash.cpp,
+    PrepareDflashInputs): the target tokens scored this step per request, how many were
+    rejected, the sampled / next-prefill token of each request state and the block tables."""
+    idx_mapping: np.ndarray             # int32 [N] request state of each batch row
+    target_query_start_loc: np.ndarray  # int32 [N+1]
+    num_rejected: np.ndarray            # int32 [N]
+    num_sampled: np.ndarray             # int32 [N]
+    last_sampled: np.ndarray            # int32 [max_num_reqs] per request state
+    next_prefill_tokens: np.ndarray     # int32 [max_num_reqs] per request state
+    target_positions: np.ndarray        # int64 [num_target_tokens]
+    block_table: np.ndarray             # int32 [N, stride]
+    num_query_per_req: int
+    num_speculative_steps: int
+    block_size: int
+    max_num_reqs: int
+    max_num_tokens: int
+    max_model_len: int
+    parallel_drafting_token_id: int
+    sample_from_anchor: bool
+
+    def scalars(self) -> dict:
+        return dict(num_query_per_req=self.num_query_per_req, num_speculative_steps=self.num_speculative_steps,
+                    block_size=self.block_size, max_num_reqs=self.max_num_reqs, max_num_tokens=self.max_num_tokens,
+                    max_model_len=self.max_model_len, parallel_drafting_token_id=self.parallel_drafting_token_id,
+                    sample_from_anchor=self.sample_from_anchor)
+
+
+def make_prepare_batch(seed: int, num_reqs: int, block: int = 16, sample_from_anchor: bool = False,
+                       prefill_frac: float = 0.25, max_prefill_chunk: int = 512, max_start: int = 30000,
+                       block_size: int = 16, max_model_len: int = 32768, stride: int | None = None,
+                       max_num_reqs: int | None = None, max_num_tokens: int | None = None,
+                       vocab: int = 151936) -> PrepareBatch:
+    """Draws a batch: each request is a decode step (the target scored the previous block of up
+    to `block` tokens and rejected some of them) or, with probability prefill_frac, a prefill
+    chunk (nothing rejected, sampled only if it was the last chunk). Positions continue a
+    context of a uniformly drawn length below max_start; request states are a random subset of
+    max_num_reqs; page ids are distinct and shuffled."""
+    n = int(num_reqs)
+    max_num_reqs = n + 3 if max_num_reqs is None else int(max_num_reqs)
+    max_num_tokens = n * block + 5 if max_num_tokens is None else int(max_num_tokens)
+    if stride is None:
+        stride = (max_start + max_prefill_chunk + 2 * block + block_size - 1) // block_size
+    u = uniform(seed, STREAM_PREP, 0, 5 * n)
+    counts = np.zeros(n, dtype=np.int64)
+    rejected = np.zeros(n, dtype=np.int64)
+    sampled = np.zeros(n, dtype=np.int64)
+    start = np.zeros(n, dtype=np.int64)
+    for r in range(n):
+        a, b_, c_, d_, e_ = u[5 * r:5 * r + 5]
+        start[r] = int(d_ * max_start)
+        if a < prefill_frac:
+            counts[r] = 1 + int(b_ * (max_prefill_chunk - 1))
+            sampled[r] = 1 if c_ < 0.5 else 0
+        else:
+            counts[r] = 1 + int(b_ * (block - 1e-9))
+            rejected[r] = int(c_ * (counts[r] - 1e-9))
+            sampled[r] = 1 if e_ < 0.9 else 0
+    qsl = np.zeros(n + 1, dtype=np.int64)
+    qsl[1:] = np.cumsum(counts)
+    positions = np.concatenate([start[r] + np.arange(counts[r]) for r in range(n)]).astype(np.int64)
+    states = np.argsort(uniform(seed, STREAM_PREP + 1, 0, max_num_reqs), kind="stable")[:n]
+    tokens = (uniform(seed, STREAM_PREP + 2, 0, 2 * max_num_reqs) * vocab).astype(np.int64).clip(0, vocab - 1)
+    pages = np.argsort(uniform(seed, STREAM_PREP + 3, 0, n * stride), kind="stable").reshape(n, stride)
+    return PrepareBatch(
+        idx_mapping=states.astype(np.int32), target_query_start_loc=qsl.astype(np.int32),
+        num_rejected=rejected.astype(np.int32), num_sampled=sampled.astype(np.int32),
+        last_sampled=tokens[:max_num_reqs].astype(np.int32),
+        next_prefill_tokens=tokens[max_num_reqs:].astype(np.int32), target_positions=positions,
+        block_table=pages.astype(np.int32), num_query_per_req=block,
+        num_speculative_steps=block if sample_from_anchor else block - 1, block_size=block_size,
+        max_num_reqs=max_num_reqs, max_num_tokens=max_num_tokens, max_model_len=max_model_len,
+        parallel_drafting_token_id=vocab - 1, sample_from_anchor=bool(sample_from_anchor))
