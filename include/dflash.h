@@ -14,6 +14,10 @@
  *      only block rows are produced                (DFlashBlockAttention over the combined
  *      [context ; block] sequence, blocks rows gathered by IndexSelect; the paged variant
  *      computes only block rows).
+ * Around it, two integer steps of the same draft step: the input preparation
+ * (PrepareDflashInputs: positions, KV slots, token ids and the sample map) and the append
+ * of new context rows to a paged store with the lengths advanced on the device
+ * (AppendContextKVDevice).
  *
  * Conventions for every entry point
  *   - Pointers to tensors and metadata are DEVICE pointers owned by the caller; the
@@ -25,7 +29,8 @@
  *     holds a message (thread-local). Nothing is thrown or aborts across this boundary.
  *   - Errors found from host arguments are reported before anything is enqueued.
  *     Errors that only device metadata can reveal (bad offsets, a bounded device wait
- *     that ran out) are recorded in the workspace and read by dflash_check_error().
+ *     that ran out) are recorded in the workspace and read by dflash_check_error(), or,
+ *     for the calls that take no workspace, ORed into a caller's device status word.
  *   - Only sm_103a (GB300) devices are supported; no CPU or other-GPU fallback exists.
  */
 #ifndef DFLASH_H_
@@ -224,6 +229,92 @@ DFLASH_API int dflash_block_attention_noalloc(const dflash_bf16* q_raw, const df
                                               int hkv, int dh, int64_t total_ctx, int max_ctx_len, int max_block_len,
                                               float eps, float rope_theta, float scale, int causal, int window,
                                               int out_dtype, void* out, int flags, dflash_stream_t stream);
+
+/* Bit that dflash_paged_append and dflash_prepare_inputs OR into their `status` word. */
+enum { DFLASH_STATUS_METADATA = 2 /* a device index or length was out of range; see the call */ };
+
+/*
+ * dflash_paged_append -- append new context rows to a paged context K/V store and advance
+ * each request's stored length on the device.
+ * (qwen3_dflash.cpp, AppendContextKVDevice: the rows that follow a request's stored context
+ *  take the positions [L, L + count), are projected as PrecomputeContextKVDevice does --
+ *  k_norm over head_dim, then RopeNeox at that position, V raw -- and are scattered into
+ *  the fixed page pools; the device seq_lens then becomes L + count, so a captured graph
+ *  sees the longer context without a host copy.)
+ *
+ *   k_raw, v       bf16 [n, Hkv, Dh]  projected keys (before k_norm) and values of the new
+ *                                     rows; v may be NULL (no V write)
+ *   new_start_loc  int32 [N+1] device rows new_start_loc[r] .. new_start_loc[r+1] are request
+ *                                     r's, in position order; rows outside
+ *                                     [new_start_loc[0], new_start_loc[N]) are ignored
+ *   seq_lens       int32 [N] device   in: stored length L_r; out: L_r + count_r. The same
+ *                                     array dflash_block_attention_paged takes as ctx_lens
+ *   block_table    int32 [N, max_pages_per_req] device, page ids of each request
+ *   k_norm_w       bf16 [Dh]
+ *   k_pool, v_pool bf16 [num_pages, page_size, Hkv, Dh]: new row i of request r (position
+ *                                     p = L_r + i) goes to row p % page_size of page
+ *                                     block_table[r, p / page_size]
+ *   eps, rope_theta                   as dflash_context_kv (same kernel arithmetic)
+ *   status         int32 device word or NULL. The call ORs DFLASH_STATUS_METADATA into it
+ *                  when a row's page index is past the table or its page id outside the
+ *                  pool (that row is not written; the length still grows), or when
+ *                  new_start_loc is not nondecreasing within [0, n] (then no length moves).
+ *                  The call never clears it.
+ *   Dh in {64, 128}; any page_size >= 1. Two launches: the rows, then the lengths (which
+ *   waits for the rows, so every row sees the old length). Allocates nothing.
+ */
+DFLASH_API int dflash_paged_append(const dflash_bf16* k_raw, const dflash_bf16* v, const int32_t* new_start_loc,
+                                   int32_t* seq_lens, const int32_t* block_table, const dflash_bf16* k_norm_w,
+                                   int num_reqs, int64_t n, int hkv, int dh, int page_size, int max_pages_per_req,
+                                   int64_t num_pages, float eps, float rope_theta, dflash_bf16* k_pool,
+                                   dflash_bf16* v_pool, int32_t* status, dflash_stream_t stream);
+
+/*
+ * dflash_prepare_inputs -- the draft step's input preparation, as one integer kernel.
+ * (qwen3_dflash.cpp, PrepareDflashInputs, the host form of vLLM's
+ *  _prepare_dflash_inputs_kernel.) For every request r of the batch (state
+ *  s = idx_mapping[r]; its target tokens target_query_start_loc[r] .. [r+1], of which the
+ *  last num_rejected[r] were rejected; P = position of the last accepted one):
+ *   context_positions[t] = target_positions[t], context_slot_mapping[t] = slot(r, that);
+ *   query row r*Q + k (k < Q = num_query_per_req) at position P + 1 + k: input_ids = the
+ *     bonus token (last_sampled[s] if num_sampled[r] > 0, else next_prefill_tokens[s]) for
+ *     k = 0 and parallel_drafting_token_id after; query_positions = min(P + 1 + k,
+ *     max_model_len - 1); query_slot_mapping = slot(r, P + 1 + k);
+ *   query_start_loc[r] = r*Q; seq_lens[r] = P + 1 + Q;
+ *   sample rows r*S + j (S = num_speculative_steps) for query offsets k = j + (0 when
+ *     sample_from_anchor, else 1) < Q: sample_indices = r*Q + k, sample_pos = P + 1 + k
+ *     (+1 when sample_from_anchor), sample_idx_mapping = s; later rows of the request 0.
+ *  with slot(r, p) = block_table[r, min(p / block_size, stride - 1)] * block_size +
+ *  p % block_size. Past the live requests: query_start_loc = N*Q, seq_lens 0, sample rows
+ *  (0, 0, -1), query_slot_mapping -1; context entries past target_query_start_loc[N] are 0.
+ *
+ *   inputs (device): idx_mapping, num_rejected, num_sampled int32 [N];
+ *     target_query_start_loc int32 [N+1]; last_sampled, next_prefill_tokens int32
+ *     [max_num_reqs] (indexed by request state); target_positions int64
+ *     [num_target_tokens]; block_table int32 [N, block_table_stride]
+ *   outputs (device): input_ids int32 [N*Q]; query_positions int64 [N*Q]; query_start_loc
+ *     int32 [max_num_reqs+1]; seq_lens int32 [max_num_reqs]; query_slot_mapping int64
+ *     [max_num_tokens]; context_positions, context_slot_mapping int64 [num_target_tokens];
+ *     sample_indices int32, sample_pos int64, sample_idx_mapping int32 [max_num_reqs*S]
+ *   Requires N <= max_num_reqs, N*Q <= max_num_tokens and Q - (1 - sample_from_anchor) <= S
+ *   (else DFLASH_ERR_INVALID_ARG). status: int32 device word or NULL; the call ORs
+ *   DFLASH_STATUS_METADATA into it when a request state is outside [0, max_num_reqs), an
+ *   accepted end falls outside the target tokens, a position is negative or
+ *   target_query_start_loc is inconsistent (the affected entries are written as 0).
+ *   One launch; allocates nothing; every output entry is written.
+ */
+DFLASH_API int dflash_prepare_inputs(const int32_t* idx_mapping, const int32_t* target_query_start_loc,
+                                     const int32_t* num_rejected, const int32_t* num_sampled,
+                                     const int32_t* last_sampled, const int32_t* next_prefill_tokens,
+                                     const int64_t* target_positions, const int32_t* block_table,
+                                     int block_table_stride, int num_reqs, int64_t num_target_tokens,
+                                     int num_query_per_req, int num_speculative_steps, int block_size,
+                                     int max_num_reqs, int max_num_tokens, int64_t max_model_len,
+                                     int parallel_drafting_token_id, int sample_from_anchor, int32_t* input_ids,
+                                     int64_t* query_positions, int32_t* query_start_loc, int32_t* seq_lens,
+                                     int64_t* query_slot_mapping, int64_t* context_positions,
+                                     int64_t* context_slot_mapping, int32_t* sample_indices, int64_t* sample_pos,
+                                     int32_t* sample_idx_mapping, int32_t* status, dflash_stream_t stream);
 
 /*
  * Reads the device error word the last dflash_block_attention call on this workspace

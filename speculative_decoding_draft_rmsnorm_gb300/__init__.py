@@ -7,6 +7,8 @@ PyTorch fallback: if the library cannot be built or loaded, every call raises.
 
 Entry points mirror include/dflash.h:
     context_kv(...)          -> dflash_context_kv
+    paged_append(...)        -> dflash_paged_append
+    prepare_inputs(...)      -> dflash_prepare_inputs
     block_attention(...)     -> dflash_block_attention
     workspace_size(...)      -> dflash_block_attention_workspace_size
     check_error(workspace)   -> dflash_check_error
@@ -17,13 +19,14 @@ import ctypes
 import os
 import threading
 
-__all__ = ["load", "lib_path", "context_kv", "block_attention", "block_attention_paged", "workspace_size", "plan",
+__all__ = ["load", "lib_path", "context_kv", "paged_append", "prepare_inputs", "STATUS_METADATA", "block_attention", "block_attention_paged", "workspace_size", "plan",
            "alloc_workspace",
            "check_error", "DFlashError", "OUT_BF16", "OUT_F32", "FLAG_FORCE_SPLIT", "FLAG_NO_SPLIT",
            "ERR_INVALID_ARG", "ERR_UNSUPPORTED", "ERR_WORKSPACE", "ERR_CUDA", "ERR_DEVICE_TIMEOUT",
            "ERR_DEVICE_METADATA"]
 
 OUT_BF16, OUT_F32 = 0, 1
+STATUS_METADATA = 2  # bit ORed into the status word of paged_append / prepare_inputs
 FLAG_FORCE_SPLIT, FLAG_NO_SPLIT = 1, 2
 ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_WORKSPACE, ERR_CUDA, ERR_DEVICE_TIMEOUT, ERR_DEVICE_METADATA = \
     -1, -2, -3, -4, -5, -6
@@ -75,6 +78,11 @@ def load(build_if_missing: bool = True):
         lib.dflash_block_attention_plan.argtypes = [I32, I64, I32, I32, I32, I64, I32, I32, I32, I32, I32, I32, P]
         lib.dflash_check_error.restype = I32
         lib.dflash_check_error.argtypes = [P, P]
+        lib.dflash_paged_append.restype = I32
+        lib.dflash_paged_append.argtypes = [P] * 6 + [I32, I64, I32, I32, I32, I32, I64, F32, F32, P, P, P, P]
+        lib.dflash_prepare_inputs.restype = I32
+        lib.dflash_prepare_inputs.argtypes = ([P] * 8 + [I32, I32, I64, I32, I32, I32, I32, I32, I64, I32, I32] +
+                                              [P] * 12)
         _lib = lib
         return lib
 
@@ -128,6 +136,90 @@ def context_kv(k_raw, ctx_pos, k_norm_w, ctx_k, *, v=None, ctx_v=None, slot=None
     rc = load().dflash_context_kv(_ptr(k_raw), _ptr(v), _ptr(ctx_pos), _ptr(k_norm_w), _ptr(slot), n, hkv, dh,
                                   float(eps), float(theta), _ptr(ctx_k), _ptr(ctx_v), ctx_k.shape[0], _stream(stream))
     _raise(rc)
+
+
+def paged_append(k_raw, new_start_loc, seq_lens, block_table, k_norm_w, k_pool, *, v=None, v_pool=None,
+                 status=None, eps=1e-6, theta=1e6, stream=None) -> None:
+    """Appends the new rows of every request to its pages and advances seq_lens on the device.
+
+    k_raw / v [n, Hkv, Dh] bf16; new_start_loc [N+1], seq_lens [N] (in/out), block_table
+    [N, max_pages] int32; k_pool / v_pool [num_pages, page_size, Hkv, Dh] bf16; status: an
+    optional int32 device word that receives STATUS_METADATA on bad metadata.
+    """
+    import torch
+    n, hkv, dh = k_raw.shape
+    nr = new_start_loc.shape[0] - 1
+    _check_tensor("k_raw", k_raw, torch.bfloat16)
+    _check_tensor("v", v, torch.bfloat16, (n, hkv, dh))
+    _check_tensor("new_start_loc", new_start_loc, torch.int32, (nr + 1,))
+    _check_tensor("seq_lens", seq_lens, torch.int32, (nr,))
+    _check_tensor("block_table", block_table, torch.int32)
+    _check_tensor("k_norm_w", k_norm_w, torch.bfloat16, (dh,))
+    _check_tensor("k_pool", k_pool, torch.bfloat16)
+    _check_tensor("v_pool", v_pool, torch.bfloat16, None if v_pool is None else tuple(k_pool.shape))
+    _check_tensor("status", status, torch.int32, (1,))
+    if k_pool.dim() != 4 or tuple(k_pool.shape[2:]) != (hkv, dh):
+        raise ValueError("k_pool must be [num_pages, page_size, Hkv, Dh]")
+    if block_table.dim() != 2 or block_table.shape[0] != nr:
+        raise ValueError("block_table must be [N, max_pages_per_req]")
+    if (v is None) != (v_pool is None):
+        raise ValueError("pass v and v_pool together")
+    rc = load().dflash_paged_append(
+        _ptr(k_raw), _ptr(v), _ptr(new_start_loc), _ptr(seq_lens), _ptr(block_table), _ptr(k_norm_w), nr, n, hkv,
+        dh, k_pool.shape[1], block_table.shape[1], k_pool.shape[0], float(eps), float(theta), _ptr(k_pool),
+        _ptr(v_pool), _ptr(status), _stream(stream))
+    _raise(rc)
+
+
+PREPARE_OUTPUTS = ("input_ids", "query_positions", "query_start_loc", "seq_lens", "query_slot_mapping",
+                   "context_positions", "context_slot_mapping", "sample_indices", "sample_pos", "sample_idx_mapping")
+
+
+def prepare_inputs(idx_mapping, target_query_start_loc, num_rejected, num_sampled, last_sampled,
+                   next_prefill_tokens, target_positions, block_table, *, num_query_per_req, num_speculative_steps,
+                   block_size, max_num_reqs, max_num_tokens, max_model_len, parallel_drafting_token_id,
+                   sample_from_anchor, out=None, status=None, stream=None) -> dict:
+    """The draft step's prepared inputs (dict of device tensors named as PREPARE_OUTPUTS).
+
+    idx_mapping, num_rejected, num_sampled [N], target_query_start_loc [N+1], last_sampled,
+    next_prefill_tokens [max_num_reqs], block_table [N, stride]: int32; target_positions int64.
+    `out` may hold preallocated outputs (same names), e.g. for graph capture.
+    """
+    import torch
+    n = idx_mapping.shape[0]
+    dev = idx_mapping.device
+    n_tgt = target_positions.shape[0]
+    nq, ns = int(num_query_per_req), int(num_speculative_steps)
+    for name, ten, shp in [("idx_mapping", idx_mapping, (n,)), ("target_query_start_loc", target_query_start_loc,
+                                                               (n + 1,)),
+                           ("num_rejected", num_rejected, (n,)), ("num_sampled", num_sampled, (n,)),
+                           ("last_sampled", last_sampled, (max_num_reqs,)),
+                           ("next_prefill_tokens", next_prefill_tokens, (max_num_reqs,)),
+                           ("block_table", block_table, None)]:
+        _check_tensor(name, ten, torch.int32, shp)
+    _check_tensor("target_positions", target_positions, torch.int64, (n_tgt,))
+    _check_tensor("status", status, torch.int32, (1,))
+    if block_table.dim() != 2 or block_table.shape[0] < n:
+        raise ValueError("block_table must be [>= N, stride]")
+    i32, i64 = torch.int32, torch.int64
+    spec = {"input_ids": (i32, n * nq), "query_positions": (i64, n * nq), "query_start_loc": (i32, max_num_reqs + 1),
+            "seq_lens": (i32, max_num_reqs), "query_slot_mapping": (i64, max_num_tokens),
+            "context_positions": (i64, n_tgt), "context_slot_mapping": (i64, n_tgt),
+            "sample_indices": (i32, max_num_reqs * ns), "sample_pos": (i64, max_num_reqs * ns),
+            "sample_idx_mapping": (i32, max_num_reqs * ns)}
+    out = dict(out or {})
+    for k, (dt, size) in spec.items():
+        if k not in out:
+            out[k] = torch.empty(size, dtype=dt, device=dev)
+        _check_tensor(k, out[k], dt, (size,))
+    rc = load().dflash_prepare_inputs(
+        _ptr(idx_mapping), _ptr(target_query_start_loc), _ptr(num_rejected), _ptr(num_sampled), _ptr(last_sampled),
+        _ptr(next_prefill_tokens), _ptr(target_positions), _ptr(block_table), block_table.stride(0), n, n_tgt, nq,
+        ns, int(block_size), int(max_num_reqs), int(max_num_tokens), int(max_model_len),
+        int(parallel_drafting_token_id), int(bool(sample_from_anchor)), *[_ptr(out[k]) for k in PREPARE_OUTPUTS],
+        _ptr(status), _stream(stream))
+    _raise(rc)
+    return out
 
 
 def workspace_size(num_reqs, total_q, hq, hkv, dh, total_ctx, max_ctx_len, max_block_len, causal=False, window=0,

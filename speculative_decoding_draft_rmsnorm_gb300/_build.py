@@ -17,7 +17,7 @@ OBJ_DIR = os.path.join(PKG, "_build")
 LIB_DIR = os.path.join(PKG, "_lib")
 LIB_NAME = "libdflash_gb300.so"
 LIB_PATH = os.path.join(LIB_DIR, LIB_NAME)
-SOURCES = ["api.cu", "attention.cu", "norm_rope.cu", "noalloc.cu"]
+SOURCES = ["api.cu", "attention.cu", "norm_rope.cu", "noalloc.cu", "draft_step.cu"]
 HEADERS = ["ptx.cuh", "internal.h", "norm_rope.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",

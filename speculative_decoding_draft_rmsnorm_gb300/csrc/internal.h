@@ -50,6 +50,21 @@ struct NormRopeJob {
 
 cudaError_t launch_norm_rope(const NormRopeJob& job, int dh, int num_sms, cudaStream_t stream);
 
+// Paged append: new row t belongs to request r when new_start_loc[r] <= t < new_start_loc[r+1];
+// it takes position seq_lens[r] + (t - new_start_loc[r]) and lands at row position % page_size
+// of page block_table[r, position / page_size] of the pool.
+struct AppendMap {
+  const int32_t* new_start_loc;  // [num_reqs + 1]
+  const int32_t* seq_lens;       // [num_reqs], the lengths before this append
+  const int32_t* block_table;    // [num_reqs, max_pages]
+  int num_reqs, max_pages, page_size;
+  int64_t num_pages;
+};
+
+// Norm + rope of the job's rows (pos and slot unused) into the rows the map gives.
+cudaError_t launch_append_rows(const NormRopeJob& job, const AppendMap& map, int dh, int num_sms,
+                               cudaStream_t stream);
+
 // Work items (warp tasks) per token of a norm+rope job: heads are taken in chunks of
 // 4 * 32 / (Dh / 8) per item.
 inline int norm_rope_items_per_token(const NormRopeJob& job, int dh) {

@@ -38,4 +38,27 @@ cudaError_t launch_norm_rope(const NormRopeJob& job, int dh, int num_sms, cudaSt
   return cudaGetLastError();
 }
 
+template <int DH>
+__global__ void __launch_bounds__(256) append_rows_kernel(const __grid_constant__ NormRopeJob job,
+                                                          const __grid_constant__ AppendMap map) {
+  const int64_t warp_id = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int64_t n_warps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+  norm_rope_rows<DH, true, true>(job, warp_id, n_warps, &map);
+}
+
+cudaError_t launch_append_rows(const NormRopeJob& job, const AppendMap& map, int dh, int num_sms,
+                               cudaStream_t stream) {
+  if (job.n_tok <= 0) return cudaSuccess;
+  const int64_t warps_needed = job.n_tok * norm_rope_items_per_token(job, dh);
+  int64_t blocks = (warps_needed + 7) / 8;
+  const int64_t cap = static_cast<int64_t>(num_sms) * 4;
+  if (blocks > cap) blocks = cap;
+  if (dh == 128) {
+    append_rows_kernel<128><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(job, map);
+  } else {
+    append_rows_kernel<64><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(job, map);
+  }
+  return cudaGetLastError();
+}
+
 }  // namespace dflash

@@ -40,12 +40,33 @@ __device__ __forceinline__ float rope_turns(int pos, float hi, float lo) {
   return t - rintf(t);
 }
 
+// Row t of a paged append: 1 = mapped to (pos, dst); 0 = in no request (ignored); -1 = past
+// the request's block table or outside the pool (reported, not written).
+__device__ __forceinline__ int append_row(const AppendMap& m, int64_t t, int* pos, int64_t* dst) {
+  int lo = 0, hi = m.num_reqs + 1;  // first i with new_start_loc[i] > t
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (m.new_start_loc[mid] <= t) lo = mid + 1; else hi = mid;
+  }
+  const int r = lo - 1;
+  if (r < 0 || r >= m.num_reqs) return 0;
+  const int64_t p = static_cast<int64_t>(m.seq_lens[r]) + (t - m.new_start_loc[r]);
+  if (p < 0 || p / m.page_size >= m.max_pages || p > 0x7fffffff) return -1;
+  const int page = m.block_table[static_cast<int64_t>(r) * m.max_pages + p / m.page_size];
+  if (page < 0 || page >= m.num_pages) return -1;
+  *pos = static_cast<int>(p);
+  *dst = static_cast<int64_t>(page) * m.page_size + p % m.page_size;
+  return 1;
+}
+
 // Work item: one token and a chunk of up to RPS * kUnroll of its heads in one part. The
 // chunk's loads (and V loads) are all issued before any arithmetic, so a warp keeps
 // kUnroll 16-byte loads per lane in flight; items are spread over all warps of the grid.
-// HAS_V = false drops the optional V copy (and its registers).
-template <int DH, bool HAS_V = true>
-__device__ __forceinline__ void norm_rope_rows(const NormRopeJob& job, int64_t warp_id, int64_t n_warps) {
+// HAS_V = false drops the optional V copy (and its registers). APPEND takes each row's
+// position and destination from *app instead of job.pos / job.slot.
+template <int DH, bool HAS_V = true, bool APPEND = false>
+__device__ __forceinline__ void norm_rope_rows(const NormRopeJob& job, int64_t warp_id, int64_t n_warps,
+                                               const AppendMap* app = nullptr) {
   constexpr int LR = DH / 8;       // lanes per row
   constexpr int HL = LR / 2;       // lanes per half row
   constexpr int RPS = 32 / LR;     // rows per warp step
@@ -80,7 +101,14 @@ __device__ __forceinline__ void norm_rope_rows(const NormRopeJob& job, int64_t w
     const NormRopePart& P = job.part[p];
     const int hc = (p == 0 ? c : c - chunks0) * HPI;
     int64_t dst_row = t;
-    if (job.slot) {
+    int pos = 0;
+    if constexpr (APPEND) {
+      const int m = append_row(*app, t, &pos, &dst_row);
+      if (m <= 0) {
+        if (m < 0 && lane == 0 && job.err) atomicOr(job.err, kErrMetadata);
+        continue;
+      }
+    } else if (job.slot) {
       const int32_t sl = job.slot[t];
       if (sl < 0 || sl >= job.capacity) {
         if (lane == 0 && job.err) atomicOr(job.err, kErrMetadata);
@@ -113,7 +141,7 @@ __device__ __forceinline__ void norm_rope_rows(const NormRopeJob& job, int64_t w
         w_pa[2 * e + 1] = bf16hi_to_f32(bv[e]);
       }
     }
-    const int pos = job.pos[t];
+    if constexpr (!APPEND) pos = job.pos[t];
     float mc[FPL], ms[FPL];  // this lane's frequencies lane * FPL + i
 #pragma unroll
     for (int i = 0; i < FPL; ++i) sincospif(2.0f * rope_turns(pos, thi[i], tlo[i]), &ms[i], &mc[i]);

@@ -73,3 +73,44 @@ def test_context_kv_rejects_bad_host_arguments():
     assert lib.dflash_context_kv(fake, None, fake, fake, None, 11, 2, 64, 1e-6, 1e6, fake, None, 10, None) == \
         D.ERR_INVALID_ARG
     assert lib.dflash_context_kv(fake, None, fake, fake, None, 0, 2, 64, 1e-6, 1e6, fake, None, 10, None) == 0
+
+
+def test_header_declares_the_draft_step_entry_points():
+    names = declared_symbols()
+    assert "dflash_paged_append" in names and "dflash_prepare_inputs" in names
+
+
+def test_paged_append_rejects_bad_host_arguments():
+    lib = D.load()
+    f = ctypes.c_void_p(256)
+
+    def call(n_req=2, n=8, hkv=2, dh=64, ps=16, max_pages=4, pages=8, eps=1e-6, theta=1e6):
+        return lib.dflash_paged_append(f, f, f, f, f, f, n_req, n, hkv, dh, ps, max_pages, pages, eps, theta, f, f,
+                                       None, None)
+
+    assert call(dh=96) == D.ERR_UNSUPPORTED
+    assert call(ps=0) == D.ERR_INVALID_ARG
+    assert call(max_pages=0) == D.ERR_INVALID_ARG
+    assert call(hkv=0) == D.ERR_INVALID_ARG
+    assert call(n=-1) == D.ERR_INVALID_ARG
+    assert call(theta=0.0) == D.ERR_INVALID_ARG
+    assert call(n_req=0) == 0  # nothing to do, nothing enqueued
+
+
+def test_prepare_inputs_rejects_bad_host_arguments():
+    lib = D.load()
+    f = ctypes.c_void_p(256)
+
+    def call(n=4, n_tgt=40, nq=16, ns=15, bs=16, max_reqs=8, max_tok=64, mml=4096, anchor=0, stride=8):
+        return lib.dflash_prepare_inputs(f, f, f, f, f, f, f, f, stride, n, n_tgt, nq, ns, bs, max_reqs, max_tok, mml,
+                                         7, anchor, *([f] * 10), None, None)
+
+    assert call(n=0) == D.ERR_INVALID_ARG
+    assert call(max_reqs=3) == D.ERR_INVALID_ARG          # more requests than request slots
+    assert call(max_tok=63) == D.ERR_INVALID_ARG          # query rows do not fit
+    assert call(ns=14) == D.ERR_INVALID_ARG               # 15 sampled rows per request, 14 steps
+    assert call(anchor=1) == D.ERR_INVALID_ARG            # sampling from the anchor: 16 rows, 15 steps
+    assert call(anchor=2) == D.ERR_INVALID_ARG
+    assert call(bs=0) == D.ERR_INVALID_ARG
+    assert call(stride=0) == D.ERR_INVALID_ARG
+    assert call(n_tgt=-1) == D.ERR_INVALID_ARG
