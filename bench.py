@@ -2,13 +2,16 @@
 """Benchmark of the DFlash draft block-attention hot path on GB300.
 
 One step = one pass of the whole path over one synthetic batch, as a draft step runs it:
-  1. dflash_context_kv: the rows appended to each request's context this step (the
-     previous block, B rows per request) are normed, rotated and scattered into the
-     device-resident context K/V store;
-  2. dflash_block_attention: q/k norm + RoPE prologue, block attention of every block
-     row over [context ; block] of its request, split-KV combine.
+  1. the rows appended to each request's context this step (the previous block, B rows
+     per request) are normed, rotated and scattered into the device-resident context K/V
+     store: dflash_context_kv with explicit slots (contiguous store), or, with --paged,
+     dflash_paged_append, which derives positions and page slots on the device and
+     advances the device lengths;
+  2. dflash_block_attention (or _paged): q/k norm + RoPE prologue, block attention of
+     every block row over [context ; block] of its request, split-KV combine.
 The context store is device state that persists across steps (it is built once,
-untimed), as the draft model keeps it resident.
+untimed), as the draft model keeps it resident. The two integer-side calls of a draft
+step (paged append, input preparation) are also timed on their own ("draft_step_ops").
 
 Metric: K/V HBM GB/s of block attention (algorithmic bytes: each allowed context or
 block key's K and V read once per (request, kv head)), with TFLOP/s and the fraction
@@ -181,8 +184,10 @@ class Step:
         self.d16, self.d32 = d16, d32
         # rows appended this step: the last min(B, C) context rows of every request
         idx = []
+        appended = np.zeros(c.num_reqs, dtype=np.int64)
         for r in range(c.num_reqs):
             a = min(int(b.block_lens[r]), int(b.ctx_lens[r]))
+            appended[r] = a
             end = int(b.ctx_start_loc[r]) + int(b.ctx_lens[r])
             idx.extend(range(end - a, end))
         self.new_idx = np.array(idx, dtype=np.int64)
@@ -211,14 +216,22 @@ class Step:
         self.host = {
             "k_new": np.ascontiguousarray(b.ctx_k_raw[self.new_idx]),
             "v_new": np.ascontiguousarray(b.ctx_v[self.new_idx]),
-            "pos_new": np.ascontiguousarray(b.ctx_pos[self.new_idx]).astype(np.int32),
-            "slot": store_row[self.new_idx].astype(np.int32),
-            "q": b.q, "k_blk": b.k_blk, "v_blk": b.v_blk, "positions": b.positions,
-            "qsl": b.query_start_loc, "csl": b.ctx_start_loc, "clen": b.ctx_lens,
+            "q": b.q, "k_blk": b.k_blk, "v_blk": b.v_blk, "positions": b.positions, "qsl": b.query_start_loc,
         }
         if page_size:
-            self.host["bt"] = self.block_table
+            # the step's append derives positions and slots on the device from the stored
+            # lengths and the block table, and advances the lengths the attention then reads
+            nsl = np.zeros(c.num_reqs + 1, dtype=np.int32)
+            nsl[1:] = np.cumsum(appended)
+            self.host.update({"nsl": nsl, "bt": self.block_table,
+                              "lens_before": (b.ctx_lens.astype(np.int64) - appended).astype(np.int32)})
+        else:
+            self.host.update({"pos_new": np.ascontiguousarray(b.ctx_pos[self.new_idx]).astype(np.int32),
+                              "slot": store_row[self.new_idx].astype(np.int32), "csl": b.ctx_start_loc,
+                              "clen": b.ctx_lens})
         self.dev = {k: (d16(v) if v.dtype == np.uint16 else d32(v)) for k, v in self.host.items()}
+        # device lengths of the paged store (the attention's ctx_lens); set by reset()
+        self.seq_lens = d32(b.ctx_lens) if page_size else None
         self.q_norm_w, self.k_norm_w = d16(b.q_norm_w), d16(b.k_norm_w)
         # the resident context store, built once (untimed): keys normed + rotated into their
         # store rows by the append kernel itself, values copied there
@@ -237,9 +250,21 @@ class Step:
         self.ws = lib.alloc_workspace(lib.workspace_size(*self.args))
         torch.cuda.synchronize()
 
+    def reset(self):
+        """Puts the stored lengths back to their value before this step's append, so that every
+        step is the same step (outside the timed events, like the L2 flush)."""
+        if self.page_size:
+            self.seq_lens.copy_(self.dev["lens_before"])
+
     def append(self, dev=None):
         d = dev or self.dev
         c = self.cfg
+        if self.page_size:
+            ps = self.page_size
+            self.lib.paged_append(d["k_new"], d["nsl"], self.seq_lens, d["bt"], self.k_norm_w,
+                                  self.ctx_k.view(-1, ps, c.hkv, c.dh), v=d["v_new"],
+                                  v_pool=self.ctx_v.view(-1, ps, c.hkv, c.dh), eps=c.eps, theta=c.theta)
+            return
         self.lib.context_kv(d["k_new"], d["pos_new"], self.k_norm_w, self.ctx_k, v=d["v_new"], ctx_v=self.ctx_v,
                             slot=d["slot"], eps=c.eps, theta=c.theta)
 
@@ -250,7 +275,7 @@ class Step:
             ps = self.page_size
             self.lib.block_attention_paged(
                 d["q"], d["k_blk"], d["v_blk"], self.ctx_k.view(-1, ps, c.hkv, c.dh),
-                self.ctx_v.view(-1, ps, c.hkv, c.dh), d["bt"], d["qsl"], d["clen"], d["positions"], self.q_norm_w,
+                self.ctx_v.view(-1, ps, c.hkv, c.dh), d["bt"], d["qsl"], self.seq_lens, d["positions"], self.q_norm_w,
                 self.k_norm_w, max_ctx_len=self.max_ctx, max_block_len=self.max_blk, out=self.out,
                 workspace=self.ws, eps=c.eps, theta=c.theta, causal=c.causal, window=c.window, flags=self.flags)
             return
@@ -260,7 +285,7 @@ class Step:
                                  theta=c.theta, causal=c.causal, window=c.window, flags=self.flags)
 
     def launches_per_step(self) -> int:
-        return 1 + int(self.plan["launches"])
+        return (2 if self.page_size else 1) + int(self.plan["launches"])
 
 
 def run_gpu(args, b: W.Batch, rank: int, world: int) -> dict | None:
@@ -286,6 +311,7 @@ def run_gpu(args, b: W.Batch, rank: int, world: int) -> dict | None:
     # ---- warm-up
     for _ in range(args.warmup):
         flush.zero_()
+        st.reset()
         st.append()
         st.attend()
     torch.cuda.synchronize()
@@ -299,6 +325,7 @@ def run_gpu(args, b: W.Batch, rank: int, world: int) -> dict | None:
         flush.zero_()
     for i in range(args.steps):
         flush.zero_()
+        st.reset()
         ev[i][0].record(stream)
         st.append()
         ev[i][1].record(stream)
@@ -318,6 +345,8 @@ def run_gpu(args, b: W.Batch, rank: int, world: int) -> dict | None:
     pinned = {k: torch.from_numpy(np.ascontiguousarray(v).view(np.int16) if v.dtype == np.uint16 else
                                   np.ascontiguousarray(v)).pin_memory() for k, v in st.host.items()}
     dev_in = {k: torch.empty(v.shape, dtype=v.dtype, device="cuda") for k, v in pinned.items()}
+    if st.page_size:  # the host copy of the lengths before the append lands in the device lengths
+        dev_in["lens_before"] = st.seq_lens
     out_host = torch.empty(st.out.shape, dtype=torch.bfloat16).pin_memory()
     h2d = sum(v.numel() * v.element_size() for v in pinned.values())
     d2h = out_host.numel() * out_host.element_size()
@@ -345,6 +374,8 @@ def run_gpu(args, b: W.Batch, rank: int, world: int) -> dict | None:
     torch.cuda.synchronize()
     e2e_ms = sum(e[0].elapsed_time(e[1]) for e in eev)
 
+    ops = time_draft_ops(lib, b, flush, stream, args.steps)
+
     peaks, peak_note = load_peaks()
     attn_avg_s = statistics.mean(attn_ms) / 1e3
     achieved = counts["kv_bytes"] / attn_avg_s / 1e9
@@ -362,7 +393,9 @@ def run_gpu(args, b: W.Batch, rank: int, world: int) -> dict | None:
         "dtype": "bf16",
         "data": "synthetic",
         "config": {**describe(cfg, b.ctx_lens),
-                   "context": (f"paged: {args.paged}-row pages in shuffled order, block table per request"
+                   "context": (f"paged: {args.paged}-row pages in shuffled order, block table per request; the "
+                               "step's append (dflash_paged_append) advances the device lengths the attention "
+                               "reads, and they are put back between steps outside the timed events"
                                if args.paged else "contiguous segments"),
                    "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"},
         "tflops": world * counts["flops"] * args.steps / (total_ms / 1e3) / 1e12,
@@ -386,8 +419,81 @@ def run_gpu(args, b: W.Batch, rank: int, world: int) -> dict | None:
         "gpu_launches": st.launches_per_step() * args.steps,
         "clocks": clk,
         "plan": st.plan,
+        "draft_step_ops": ops,
     }
     return res
+
+
+def time_draft_ops(lib, b: W.Batch, flush, stream, steps: int) -> dict:
+    """The two integer-side calls of a draft step on a batch of this workload's requests,
+    each timed on its own (CUDA events around each call, L2 flushed before each):
+
+      paged_append: every request appends B rows (the previous block) after its context
+        into 16-row pages; bytes = rows read (K and V) + rows written (K and V).
+      prepare_inputs: decode-step metadata of the same requests (each scored a block of up
+        to B target tokens and rejected some); bytes = every input and output array.
+    Both move kilobytes to a few MB, so their time is launch latency, not bandwidth.
+    """
+    import numpy as np
+    import torch
+    c = b.cfg
+    n, blk, ps = c.num_reqs, c.block, 16
+    d32 = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).cuda()  # noqa: E731
+
+    def timed(fn, reset=None):
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(steps)]
+        for _ in range(3):
+            if reset:
+                reset()
+            fn()
+        for i in range(steps):
+            flush.zero_()
+            if reset:
+                reset()
+            ev[i][0].record(stream)
+            fn()
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+        return statistics.mean(e[0].elapsed_time(e[1]) for e in ev) * 1e3  # us
+
+    # paged append: B rows per request after a context of ctx_lens[r] rows
+    lens0 = b.ctx_lens.astype(np.int64)
+    first_page = lens0 // ps
+    last_page = (lens0 + blk - 1) // ps
+    max_pages = int(last_page.max()) + 1
+    bt = np.zeros((n, max_pages), dtype=np.int32)
+    nxt = 0
+    for r in range(n):
+        for p in range(int(first_page[r]), int(last_page[r]) + 1):
+            bt[r, p] = nxt
+            nxt += 1
+    pool_k = torch.zeros((nxt, ps, c.hkv, c.dh), dtype=torch.bfloat16, device="cuda")
+    pool_v = torch.zeros_like(pool_k)
+    rows = n * blk
+    k_new = torch.randn((rows, c.hkv, c.dh), device="cuda").to(torch.bfloat16)
+    v_new = torch.randn_like(k_new)
+    w = torch.ones(c.dh, dtype=torch.bfloat16, device="cuda")
+    nsl = d32(np.arange(n + 1) * blk)
+    base, lens, dbt = d32(lens0), d32(lens0), d32(bt)
+    append_us = timed(lambda: lib.paged_append(k_new, nsl, lens, dbt, w, pool_k, v=v_new, v_pool=pool_v,
+                                               eps=c.eps, theta=c.theta), reset=lambda: lens.copy_(base))
+    append_bytes = 2 * 2 * rows * c.hkv * c.dh * 2 + (n + 1) * 4 + 2 * n * 4
+
+    # input preparation for the same requests
+    pb = W.make_prepare_batch(c.seed, n, block=blk, prefill_frac=0.0)
+    t = {k: d32(getattr(pb, k)) for k in ("idx_mapping", "target_query_start_loc", "num_rejected", "num_sampled",
+                                          "last_sampled", "next_prefill_tokens", "block_table")}
+    t["target_positions"] = torch.from_numpy(pb.target_positions.astype(np.int64)).cuda()
+    out = lib.prepare_inputs(**t, **pb.scalars())
+    prep_us = timed(lambda: lib.prepare_inputs(**t, **pb.scalars(), out=out))
+    prep_bytes = sum(v.numel() * v.element_size() for v in list(t.values()) + list(out.values()))
+    return {
+        "paged_append": {"us": append_us, "rows": rows, "bytes": append_bytes,
+                         "gb_per_s": append_bytes / (append_us * 1e-6) / 1e9, "launches": 2,
+                         "bound": "launch latency (a few MB)"},
+        "prepare_inputs": {"us": prep_us, "requests": n, "target_tokens": int(pb.target_query_start_loc[-1]),
+                           "bytes": prep_bytes, "launches": 1, "bound": "launch latency (kilobytes)"},
+    }
 
 
 # ---------------------------------------------------------------- oracle (CPU)

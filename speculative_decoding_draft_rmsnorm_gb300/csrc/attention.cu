@@ -95,12 +95,50 @@ __device__ __forceinline__ long long cta_first_tile(long long c, long long T, lo
   return static_cast<long long>(prod / static_cast<unsigned long long>(grid));
 }
 
+// Cost of key tiles and of segment starts in the balanced schedule, in eighths of a tile: a
+// CTA's time grows by about 1.25 tiles for every group it starts (the group's Q tile, the
+// previous segment's epilogue), measured per CTA on the Qwen3-4B-shaped layers.
+constexpr long long kTileCost = 8, kSegCost = 10;
+
+// First tile of CTA c (0 <= c <= grid) of the balanced schedule over T tiles in G groups
+// (req: the requests' tile and group offsets, n_req of them). With at least 4 tiles a CTA
+// the split balances tiles and segment starts: tile t of group gi starts at cost
+// u_t = 8 t + 10 (gi + 1), and CTA c takes the tiles with u_t in [c W / grid, (c+1) W / grid),
+// W = 8 T + 10 G. Consecutive tile starts are at most 18 apart and every interval spans at
+// least 31, so no CTA is empty. With fewer tiles: an even split, and with fewer tiles than
+// CTAs one tile to each of the first T CTAs; empty CTAs only ever follow the last tile.
+__device__ long long balanced_first_tile(long long c, long long T, long long G, long long grid, const ReqTiles* req,
+                                         int n_req) {
+  if (c >= grid) return T;
+  if (T < 4 * grid) return T >= grid ? cta_first_tile(c, T, grid) : (c < T ? c : T);
+  const long long W = kTileCost * T + kSegCost * G;
+  const long long w = c * W / grid;
+  auto ufirst = [&](int r) { return kTileCost * req[r].toff + kSegCost * (static_cast<long long>(req[r].goff) + 1); };
+  if (ufirst(0) > w) return 0;
+  int a = 0, z = n_req - 1;  // the last request whose first tile starts at or below w
+  while (a < z) {
+    const int m = (a + z + 1) >> 1;
+    if (ufirst(m) <= w) a = m; else z = m - 1;
+  }
+  const ReqTiles& q = req[a];
+  if (q.cnt == 0) return q.toff;
+  const long long per = kTileCost * q.n + kSegCost;  // one group: its start and its tiles
+  const long long d = w - ufirst(a);
+  const long long k = d / per;
+  if (k >= q.cnt) return q.toff + static_cast<long long>(q.cnt) * q.n;
+  const long long rem = d - k * per;
+  long long j = (rem + kTileCost - 1) / kTileCost;  // tiles of group k that start below w
+  if (j > q.n) j = q.n;
+  return q.toff + k * q.n + j;
+}
+
 // Validates the device metadata and writes one Group per (request, kv head, query tile)
 // with its key-tile count and the global index of its first tile (prefix over groups).
 // hdr[1] = number of groups, hdr[2] = total tiles. For the balanced schedule it also
-// writes each CTA's record: CTA c owns tiles [c*T/grid, (c+1)*T/grid), its first group is
-// the one holding tile c*T/grid, and the record carries that group so that the CTA's
-// first loads depend on one read.
+// writes each CTA's record: CTA c owns tiles [lo_c, lo_{c+1}) (balanced_first_tile; with
+// more than 256 requests an even split, lo_c = c*T/grid), its first group is the one
+// holding tile lo_c, and the record carries that group so that the CTA's first loads
+// depend on one read.
 //
 // One block of 256 threads. Requests are taken 256 at a time: a thread loads its request's
 // metadata (one round trip), the block scans the group and tile counts, then every thread
@@ -202,7 +240,8 @@ __device__ void build_groups(const PrologueParams& p) {
       // one thread per CTA: its range, the request holding its first tile (the last request
       // whose first tile is <= lo: that one has groups), and the group within it
       for (int c = tid; c < grid; c += blockDim.x) {
-        const long long lo = cta_first_tile(c, chunk_t, grid), hi = cta_first_tile(c + 1, chunk_t, grid);
+        const long long lo = balanced_first_tile(c, chunk_t, chunk_g, grid, s_req, p.num_reqs);
+        const long long hi = balanced_first_tile(c + 1, chunk_t, chunk_g, grid, s_req, p.num_reqs);
         int a = 0, z = p.num_reqs - 1;
         while (a < z) {
           const int m = (a + z + 1) >> 1;
@@ -1015,14 +1054,20 @@ __global__ void __launch_bounds__(256) combine_kernel(const __grid_constant__ At
   }
   const long long tt = static_cast<long long>(__ldcg(p.hdr + 2));
   const long long grid = p.grid;
-  const long long lo0 = static_cast<long long>(b) * tt / grid;  // CTA b's first tile
+  const long long lo0 = __ldcg(&p.cta_rec[b].lo);  // CTA b's first tile
   // split at this boundary, and not at an earlier one
   const bool mine = tt > 0 && G.start < lo1 && G.start >= lo0;
+  // contributors: CTAs ca = b .. cb, the last one being the last CTA whose first tile lies in
+  // the group (no CTA between is empty: empty CTAs only follow the last tile)
+  const long long ca = b;
+  long long cb = b + 1;
+  if (mine) {
+    const long long gend = static_cast<long long>(G.start) + G.n;
+    while (cb + 1 < grid && __ldcg(&p.cta_rec[cb + 1].lo) < gend) ++cb;
+  }
   grid_dependency_wait();
   if (!mine) return;
-  // contributors: CTAs ca = b .. cb; the group is CTA b's first segment iff it starts at lo0
-  auto cta_of = [&](long long t) { return ((t + 1) * grid + tt - 1) / tt - 1; };
-  const long long ca = b, cb = cta_of(static_cast<long long>(G.start) + G.n - 1);
+  // the group is CTA b's first segment iff it starts at lo0
   const bool ca_first = G.start == lo0;
   constexpr int CPR = DH / 8;   // 8-float chunks per row; block y covers rows [16y, 16y+16)
   constexpr int kMaxBatch = 2;  // contributors whose loads are in flight together
