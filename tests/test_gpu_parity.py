@@ -153,6 +153,24 @@ def test_split_and_unsplit_paths_both_match(flags):
     U.assert_close_bf16(got, want, f"flags={flags}")
 
 
+@pytest.mark.parametrize("ctx,cap", [(300, 32768), (8000, 32768), (3000, 3000)])
+def test_store_capacity_far_above_the_lengths(ctx, cap):
+    # the grid is sized from the host bounds (store capacity, max lengths); with live lengths
+    # far below them there are fewer tiles than CTAs (ctx 300 in segments of 32768: 16 tiles
+    # for 129 CTAs, every group split over 4 CTAs) or under 4 tiles a CTA (ctx 8000), where
+    # the schedule leaves the cost-balanced split; every split group must still merge from
+    # exactly its contributors
+    import dataclasses
+    import speculative_decoding_draft_rmsnorm_gb300 as lib
+    full = W.make_batch(cfg(8, 2, 128, seed=21), ctx_lens=[cap, cap], block_lens=[16, 16])
+    b = dataclasses.replace(full, ctx_lens=np.array([ctx, ctx - 1], dtype=np.int32))
+    ck = U.stored_ctx_k(b)
+    want = U.oracle_attention(b, ck)
+    plan = lib.plan(2, 32, 8, 2, 128, b.ctx_k_raw.shape[0], cap, 16)
+    got = U.dev_to_f64(U.gpu_attention(b, ck, max_ctx_len=cap))
+    U.assert_close_bf16(got, want, f"ctx {ctx} in segments of {cap} ({plan['ctas']} CTAs)")
+
+
 def test_context_slack_rows_are_never_read():
     # the segment holds more rows than ctx_lens says; the extra rows are NaN and must
     # not reach the output (neither through K scores nor through V with weight 0)

@@ -52,13 +52,14 @@ def gpu_attention(b: W.Batch, ctx_k_bits=None, ctx_k_dev=None, out_dtype=0, flag
     import speculative_decoding_draft_rmsnorm_gb300 as D
     c = b.cfg
     ck = ctx_k_dev if ctx_k_dev is not None else bf16_dev(ctx_k_bits)
-    args = dict(eps=c.eps, theta=c.theta, causal=c.causal, window=c.window)
+    args = dict(eps=c.eps, theta=c.theta, causal=c.causal, window=c.window,
+                max_ctx_len=int(max(1, b.ctx_lens.max(initial=0))))
     args.update(kw)
     return D.block_attention(
         bf16_dev(b.q), bf16_dev(b.k_blk), bf16_dev(b.v_blk), ck, bf16_dev(b.ctx_v), i32_dev(b.query_start_loc),
         i32_dev(b.ctx_start_loc), i32_dev(b.ctx_lens), i32_dev(b.positions), bf16_dev(b.q_norm_w),
-        bf16_dev(b.k_norm_w), max_ctx_len=int(max(1, b.ctx_lens.max(initial=0))),
-        max_block_len=int(max(1, b.block_lens.max(initial=0))), out_dtype=out_dtype, flags=flags, **args)
+        bf16_dev(b.k_norm_w), max_block_len=int(max(1, b.block_lens.max(initial=0))), out_dtype=out_dtype,
+        flags=flags, **args)
 
 
 def assert_close_bf16(got: np.ndarray, want: np.ndarray, what: str = "") -> None:
