@@ -88,6 +88,12 @@ __device__ __forceinline__ Group make_group(const ReqTiles& q, int k, int tpq, i
   return G;
 }
 
+// a / b for 0 <= a, 0 < b: 32-bit division when both fit
+__device__ __forceinline__ long long div_nonneg(long long a, long long b) {
+  if (a <= 0xffffffffll && b <= 0xffffffffll) return static_cast<unsigned>(a) / static_cast<unsigned>(b);
+  return a / b;
+}
+
 // floor(c * T / grid) for 0 <= c <= grid, T < 2^31: 32-bit division when the product fits
 __device__ __forceinline__ long long cta_first_tile(long long c, long long T, long long grid) {
   const unsigned long long prod = static_cast<unsigned long long>(c) * static_cast<unsigned long long>(T);
@@ -99,6 +105,7 @@ __device__ __forceinline__ long long cta_first_tile(long long c, long long T, lo
 // CTA's time grows by about 1.25 tiles for every group it starts (the group's Q tile, the
 // previous segment's epilogue), measured per CTA on the Qwen3-4B-shaped layers.
 constexpr long long kTileCost = 8, kSegCost = 10;
+static_assert(kTileCost == 8, "balanced_first_tile divides by kTileCost with a shift");
 
 // First tile of CTA c (0 <= c <= grid) of the balanced schedule over T tiles in G groups
 // (req: the requests' tile and group offsets, n_req of them). With at least 4 tiles a CTA
@@ -112,7 +119,7 @@ __device__ long long balanced_first_tile(long long c, long long T, long long G, 
   if (c >= grid) return T;
   if (T < 4 * grid) return T >= grid ? cta_first_tile(c, T, grid) : (c < T ? c : T);
   const long long W = kTileCost * T + kSegCost * G;
-  const long long w = c * W / grid;
+  const long long w = div_nonneg(c * W, grid);
   auto ufirst = [&](int r) { return kTileCost * req[r].toff + kSegCost * (static_cast<long long>(req[r].goff) + 1); };
   if (ufirst(0) > w) return 0;
   int a = 0, z = n_req - 1;  // the last request whose first tile starts at or below w
@@ -124,10 +131,10 @@ __device__ long long balanced_first_tile(long long c, long long T, long long G, 
   if (q.cnt == 0) return q.toff;
   const long long per = kTileCost * q.n + kSegCost;  // one group: its start and its tiles
   const long long d = w - ufirst(a);
-  const long long k = d / per;
+  const long long k = div_nonneg(d, per);
   if (k >= q.cnt) return q.toff + static_cast<long long>(q.cnt) * q.n;
   const long long rem = d - k * per;
-  long long j = (rem + kTileCost - 1) / kTileCost;  // tiles of group k that start below w
+  long long j = (rem + kTileCost - 1) >> 3;  // tiles of group k that start below w (kTileCost = 8)
   if (j > q.n) j = q.n;
   return q.toff + k * q.n + j;
 }
@@ -140,24 +147,31 @@ __device__ long long balanced_first_tile(long long c, long long T, long long G, 
 // holding tile lo_c, and the record carries that group so that the CTA's first loads
 // depend on one read.
 //
-// One block of 256 threads. Requests are taken 256 at a time: a thread loads its request's
-// metadata (one round trip), the block scans the group and tile counts, then every thread
-// writes the groups gi = tid, tid + 256, ... of the chunk (its request found by a search
-// over the scan in shared memory) and, with one chunk, one thread per CTA writes the CTA's
-// record, so no thread walks a request's groups serially.
-__device__ void build_groups(const PrologueParams& p) {
+// Blocks of 256 threads, `nparts` of them (even). Requests are taken 256 at a time: a thread
+// loads its request's metadata (one round trip), the block scans the group and tile counts,
+// then every thread writes groups of the chunk (its request found by a search over the scan
+// in shared memory) and, with one chunk, one thread per CTA writes the CTA's record, so no
+// thread walks a request's groups serially. With one chunk (at most 256 requests) each of
+// the nparts blocks repeats the loads and the scan; the first half of them write equal
+// shares of the groups, the second half equal shares of the records: the stores of the
+// table, not its arithmetic, set the time of this step (the L2 is full of dirty lines from
+// the previous work), so spreading them over several SMs shortens it. Only part 0 writes
+// the header words; with several chunks part 0 does all the work.
+__device__ void build_groups(const PrologueParams& p, int part, int nparts) {
   __shared__ ReqTiles s_req[256];
   __shared__ int s_cnt[256];  // inclusive scan of the chunk's group counts
   __shared__ int s_wg[8];
   __shared__ long long s_wt[8];
   __shared__ int s_bad_global;
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  const bool one_chunk = p.num_reqs <= 256;
+  if (!one_chunk && part != 0) return;
+  const bool lead = part == 0;  // writes the header words (error word, counts)
   if (tid == 0) {
-    p.hdr[0] = 0;  // error word of this call (only this block writes it before kernel B)
+    if (lead) p.hdr[0] = 0;  // error word of this call (only this block writes it before kernel B)
     s_bad_global = 0;
   }
   __syncthreads();
-  const bool one_chunk = p.num_reqs <= 256;
   const long long grid = p.grid_b;
   int run_g = 0;
   long long run_t = 0;
@@ -176,7 +190,7 @@ __device__ void build_groups(const PrologueParams& p) {
       const bool ok = q.B >= 0 && q.q0 >= 0 && q1 <= p.total_q && q.c0 >= 0 && c1 >= q.c0 && c1 <= p.total_ctx &&
                       q.C >= 0 && q.C <= c1 - q.c0 && q.C <= p.max_ctx_len && q.B <= p.max_block_len;
       if (!ok) {
-        atomicOr(&p.hdr[0], kErrMetadata);
+        if (lead) atomicOr(&p.hdr[0], kErrMetadata);
         q.B = 0;
       }
       if (q.B > 0) {
@@ -225,8 +239,19 @@ __device__ void build_groups(const PrologueParams& p) {
     s_req[tid] = q;
     __syncthreads();
     const bool fits = run_g + chunk_g <= p.groups_max && run_t + chunk_t <= 0x7fffffffLL;
-    if (!fits && tid == 0) atomicOr(&p.hdr[0], kErrMetadata);
-    for (int j = tid; fits && j < chunk_g; j += blockDim.x) {
+    if (!fits && tid == 0 && lead) atomicOr(&p.hdr[0], kErrMetadata);
+    // this part's share: with one chunk the first half of the parts write the groups and the
+    // second half the CTA records, each a contiguous share; otherwise part 0 writes all
+    const int half = nparts / 2;
+    const int gshare = one_chunk ? (chunk_g + half - 1) / half : chunk_g;
+    const int g_begin = one_chunk ? (part < half ? min(chunk_g, part * gshare) : chunk_g) : 0;
+    const int g_end = one_chunk ? min(chunk_g, g_begin + gshare) : chunk_g;
+    const int cshare = static_cast<int>((grid + half - 1) / half);
+    const int c_begin = one_chunk ? (part >= half ? min(static_cast<int>(grid), (part - half) * cshare)
+                                                  : static_cast<int>(grid))
+                                  : 0;
+    const int c_end = one_chunk ? min(static_cast<int>(grid), c_begin + cshare) : static_cast<int>(grid);
+    for (int j = g_begin + tid; fits && j < g_end; j += blockDim.x) {
       int a = 0, b = 255;  // first request of the chunk whose inclusive count exceeds j
       while (a < b) {
         const int m = (a + b) >> 1;
@@ -239,7 +264,7 @@ __device__ void build_groups(const PrologueParams& p) {
     if (one_chunk && fits && p.cta_rec != nullptr && chunk_t > 0) {
       // one thread per CTA: its range, the request holding its first tile (the last request
       // whose first tile is <= lo: that one has groups), and the group within it
-      for (int c = tid; c < grid; c += blockDim.x) {
+      for (int c = c_begin + tid; c < c_end; c += blockDim.x) {
         const long long lo = balanced_first_tile(c, chunk_t, chunk_g, grid, s_req, p.num_reqs);
         const long long hi = balanced_first_tile(c + 1, chunk_t, chunk_g, grid, s_req, p.num_reqs);
         int a = 0, z = p.num_reqs - 1;
@@ -265,18 +290,24 @@ __device__ void build_groups(const PrologueParams& p) {
   }
   if (s_bad_global || run_g > p.groups_max || run_t > 0x7fffffffLL) {
     // no work for kernel B (the last two cannot happen with valid host bounds)
-    if (tid == 0) atomicOr(&p.hdr[0], kErrMetadata);
+    if (tid == 0 && lead) atomicOr(&p.hdr[0], kErrMetadata);
     run_g = 0;
     run_t = 0;
   }
-  if (tid == 0) {
+  if (tid == 0 && lead) {
     p.hdr[1] = static_cast<uint32_t>(run_g);
     p.hdr[2] = static_cast<uint32_t>(run_t);
   }
   if (p.cta_rec == nullptr) return;
   if (run_t == 0) {
-    // records written above (if any) are replaced: no CTA has work
-    for (int c = tid; c < grid; c += blockDim.x) p.cta_rec[c] = CtaRecord{};
+    // records written above (if any) are replaced: no CTA has work. Each part clears the
+    // records it wrote (with several chunks part 0 is the only part and owns all of them).
+    const int half = nparts / 2;
+    const long long share = (grid + half - 1) / half;
+    const long long lo_c = part >= half ? static_cast<long long>(part - half) * share : grid;
+    const int c0 = one_chunk ? static_cast<int>(lo_c < grid ? lo_c : grid) : 0;
+    const int c1 = one_chunk ? static_cast<int>(c0 + share < grid ? c0 + share : grid) : static_cast<int>(grid);
+    for (int c = c0 + tid; c < c1; c += blockDim.x) p.cta_rec[c] = CtaRecord{};
     return;
   }
   if (!one_chunk) {
@@ -303,17 +334,21 @@ __device__ void build_groups(const PrologueParams& p) {
   }
 }
 
-// Three blocks per SM (at most 85 registers a thread), so that the launch below, sized to
-// one item per warp where it can be, is resident at once.
+// Blocks 0 .. kTableBlocks-1 build the group table and the CTA records; the others run the
+// q / block-k norm + RoPE. Three blocks per SM (at most 85 registers a thread), so that the
+// launch below, sized to one item per warp where it can be, is resident at once.
+constexpr int kTableBlocks = 8;
+static_assert(kTableBlocks % 2 == 0, "half the table blocks write groups, half write records");
+
 template <int DH>
 __global__ void __launch_bounds__(256, 3) prologue_kernel(const __grid_constant__ PrologueParams p) {
   grid_dependents_launch();
-  if (blockIdx.x == 0) {
-    build_groups(p);
+  if (blockIdx.x < kTableBlocks) {
+    build_groups(p, static_cast<int>(blockIdx.x), kTableBlocks);
     return;
   }
-  const int64_t warp_id = (static_cast<int64_t>(blockIdx.x - 1) * blockDim.x + threadIdx.x) >> 5;
-  const int64_t n_warps = (static_cast<int64_t>(gridDim.x - 1) * blockDim.x) >> 5;
+  const int64_t warp_id = (static_cast<int64_t>(blockIdx.x - kTableBlocks) * blockDim.x + threadIdx.x) >> 5;
+  const int64_t n_warps = (static_cast<int64_t>(gridDim.x - kTableBlocks) * blockDim.x) >> 5;
   norm_rope_rows<DH, false>(p.job, warp_id, n_warps);
 }
 
@@ -1311,8 +1346,8 @@ cudaError_t launch_attention(const AttnHost& h, cudaStream_t stream, char* msg, 
   pp.paged_cap = h.paged ? h.max_pages * h.page_size : 0;
   cudaError_t e = cudaSuccess;
   int64_t nr_blocks = (h.total_q * norm_rope_items_per_token(pp.job, h.dh) + 7) / 8;
-  nr_blocks = std::min<int64_t>(nr_blocks, static_cast<int64_t>(h.num_sms) * 3 - 1);  // all co-resident
-  const unsigned grid_a = static_cast<unsigned>(1 + nr_blocks);
+  nr_blocks = std::min<int64_t>(nr_blocks, static_cast<int64_t>(h.num_sms) * 3 - kTableBlocks);  // all co-resident
+  const unsigned grid_a = static_cast<unsigned>(kTableBlocks + nr_blocks);
   if (h.dh == 128)
     prologue_kernel<128><<<grid_a, 256, 0, stream>>>(pp);
   else
