@@ -38,12 +38,22 @@ cudaError_t launch_norm_rope(const NormRopeJob& job, int dh, int num_sms, cudaSt
   return cudaGetLastError();
 }
 
+// Start locations of up to this many requests are staged in shared memory for the row search.
+constexpr int kAppendSmemReqs = 1024;
+
 template <int DH>
 __global__ void __launch_bounds__(256) append_rows_kernel(const __grid_constant__ NormRopeJob job,
                                                           const __grid_constant__ AppendMap map) {
+  __shared__ int32_t s_nsl[kAppendSmemReqs + 1];
+  AppendMap m = map;
+  if (map.num_reqs <= kAppendSmemReqs) {
+    for (int i = threadIdx.x; i <= map.num_reqs; i += blockDim.x) s_nsl[i] = map.new_start_loc[i];
+    __syncthreads();
+    m.new_start_loc = s_nsl;
+  }
   const int64_t warp_id = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int64_t n_warps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
-  norm_rope_rows<DH, true, true>(job, warp_id, n_warps, &map);
+  norm_rope_rows<DH, true, true>(job, warp_id, n_warps, &m);
 }
 
 cudaError_t launch_append_rows(const NormRopeJob& job, const AppendMap& map, int dh, int num_sms,

@@ -100,6 +100,19 @@ __device__ __forceinline__ void norm_rope_rows(const NormRopeJob& job, int64_t w
     const int p = c < chunks0 ? 0 : 1;
     const NormRopePart& P = job.part[p];
     const int hc = (p == 0 ? c : c - chunks0) * HPI;
+    // issue every load of the item first
+    uint4 raw[kUnroll], vraw[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int h = hc + u * RPS + row_in_step;
+      raw[u] = make_uint4(0, 0, 0, 0);
+      vraw[u] = make_uint4(0, 0, 0, 0);
+      if (h < P.heads) {
+        raw[u] = *reinterpret_cast<const uint4*>(P.src + (t * P.heads + h) * DH + elem0);
+        if (HAS_V && P.v_src) vraw[u] = *reinterpret_cast<const uint4*>(P.v_src + (t * P.heads + h) * DH + elem0);
+      }
+    }
+    // the row's destination (and, appending, its position) while its loads are in flight
     int64_t dst_row = t;
     int pos = 0;
     if constexpr (APPEND) {
@@ -115,18 +128,6 @@ __device__ __forceinline__ void norm_rope_rows(const NormRopeJob& job, int64_t w
         continue;
       }
       dst_row = sl;
-    }
-    // issue every load of the item first
-    uint4 raw[kUnroll], vraw[kUnroll];
-#pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
-      const int h = hc + u * RPS + row_in_step;
-      raw[u] = make_uint4(0, 0, 0, 0);
-      vraw[u] = make_uint4(0, 0, 0, 0);
-      if (h < P.heads) {
-        raw[u] = *reinterpret_cast<const uint4*>(P.src + (t * P.heads + h) * DH + elem0);
-        if (HAS_V && P.v_src) vraw[u] = *reinterpret_cast<const uint4*>(P.v_src + (t * P.heads + h) * DH + elem0);
-      }
     }
     float w_me[8], w_pa[8];
     {
