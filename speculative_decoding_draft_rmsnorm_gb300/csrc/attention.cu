@@ -1242,10 +1242,6 @@ WorkspacePlan plan_workspace(int num_reqs, int64_t total_q, int hq, int hkv, int
   } else {
     w.grid = std::min(num_sms, w.groups_max);
   }
-  if (const char* e = std::getenv("DFLASH_GRID")) {  // tuning sweeps
-    const int v = std::atoi(e);
-    if (v > 0) w.grid = std::min(v, num_sms);
-  }
   w.grid = std::max(1, w.grid);
   w.parts = w.balanced ? 2 * w.grid : 0;
   size_t off = 0;
