@@ -346,3 +346,36 @@ def test_prepare_inputs_graph_replay_with_new_values():
     want = _prep_oracle(pb2)
     for k in want:
         assert np.array_equal(out[k].cpu().numpy(), want[k]), k
+
+
+def test_prepare_inputs_context_arrays_longer_than_the_scored_tokens():
+    pb = W.make_prepare_batch(10, 6)
+    n_tgt = int(pb.target_query_start_loc[-1])
+    pb.target_positions = np.concatenate([pb.target_positions, np.full(9, 777, dtype=np.int64)])
+    want = oracle.prepare_dflash_inputs(pb.idx_mapping, pb.target_query_start_loc, pb.num_rejected, pb.num_sampled,
+                                        pb.last_sampled, pb.next_prefill_tokens, pb.target_positions, pb.block_table,
+                                        num_target_tokens=n_tgt + 9, **pb.scalars())
+    got = _prep_gpu(pb)
+    for k in want:
+        assert np.array_equal(got[k], want[k]), k
+
+
+def test_paged_append_without_values_writes_keys_only():
+    import torch
+    hkv, dh, ps, n_req = 2, 128, 16, 3
+    lens = np.array([5, 0, 40], dtype=np.int32)
+    counts = np.array([16, 3, 16])
+    bt, pk, pv, nsl = _store(n_req, lens, counts, ps, 5, hkv, dh, seed=12)
+    n = int(nsl[-1])
+    k_raw = W.normal_bf16(13, 0, n * hkv * dh).reshape(n, hkv, dh)
+    w = W.uniform_bf16(13, 2, dh, 0.5, 1.5)
+    want_k, _, want_lens, _ = oracle.paged_append(pk, pv, bt, lens, nsl, k_raw, None, w, ps)
+    dk, dl = U.bf16_dev(pk), U.i32_dev(lens)
+    D().paged_append(U.bf16_dev(k_raw), U.i32_dev(nsl), dl, U.i32_dev(bt), U.bf16_dev(w), dk)
+    torch.cuda.synchronize()
+    assert dl.cpu().numpy().tolist() == want_lens.tolist()
+    got_k = U.dev_bits(dk).reshape(pk.shape)
+    written = ~np.all(want_k == NAN_BF16, axis=(2, 3))
+    assert written.sum() == n
+    assert np.array_equal(got_k[~written], want_k[~written])
+    assert np.mean(got_k[written] == want_k[written]) > 0.999

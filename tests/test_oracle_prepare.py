@@ -138,3 +138,17 @@ def test_more_sampled_rows_than_steps_and_negative_positions_are_rejected():
     kw["target_positions"][0] = -1
     with pytest.raises(PrepareError):
         _run(**kw)
+
+
+def test_context_arrays_longer_than_the_scored_tokens_end_in_zeros():
+    # a caller may size the context arrays for a larger batch; entries past the last request's
+    # tokens belong to no request and are written as 0
+    b = W.make_prepare_batch(4, 5)
+    n_tgt = int(b.target_query_start_loc[-1])
+    kw = dict(b.__dict__)
+    kw["target_positions"] = np.concatenate([b.target_positions, np.full(7, 12345, dtype=np.int64)])
+    o = _run(**kw, num_target_tokens=n_tgt + 7)
+    base = _run(**b.__dict__)
+    assert np.array_equal(o["context_positions"][:n_tgt], base["context_positions"])
+    assert np.array_equal(o["context_slot_mapping"][:n_tgt], base["context_slot_mapping"])
+    assert np.all(o["context_positions"][n_tgt:] == 0) and np.all(o["context_slot_mapping"][n_tgt:] == 0)
