@@ -171,6 +171,21 @@ def test_store_capacity_far_above_the_lengths(ctx, cap):
     U.assert_close_bf16(got, want, f"ctx {ctx} in segments of {cap} ({plan['ctas']} CTAs)")
 
 
+@pytest.mark.parametrize("flags", [0, 1, 2])
+def test_more_than_256_requests(flags):
+    # the schedule is built 256 requests at a time past 256 requests (an even split of the tiles)
+    rng = np.random.default_rng(23)
+    n = 300
+    ctx = rng.integers(0, 400, n)
+    ctx[::17] = 0
+    blk = rng.integers(1, 17, n)
+    b = W.make_batch(cfg(8, 2, 64, seed=23), ctx_lens=ctx, block_lens=blk)
+    ck = U.stored_ctx_k(b)
+    want = U.oracle_attention(b, ck)
+    got = U.dev_to_f64(U.gpu_attention(b, ck, flags=flags))
+    U.assert_close_bf16(got, want, f"300 requests flags={flags}")
+
+
 def test_context_slack_rows_are_never_read():
     # the segment holds more rows than ctx_lens says; the extra rows are NaN and must
     # not reach the output (neither through K scores nor through V with weight 0)
