@@ -379,3 +379,30 @@ def test_paged_append_without_values_writes_keys_only():
     assert written.sum() == n
     assert np.array_equal(got_k[~written], want_k[~written])
     assert np.mean(got_k[written] == want_k[written]) > 0.999
+
+
+def test_paged_append_more_requests_than_staged_start_locations():
+    # past 1024 requests the row kernel searches the start locations in global memory, and the
+    # length kernel's one block loops over the requests
+    import torch
+    hkv, dh, ps, n_req = 1, 64, 16, 1100
+    rng = np.random.default_rng(31)
+    lens = rng.integers(0, 40, n_req).astype(np.int32)
+    counts = rng.integers(0, 3, n_req)
+    bt, pk, pv, nsl = _store(n_req, lens, counts, ps, 3, hkv, dh, seed=32)
+    n = int(nsl[-1])
+    k_raw = W.normal_bf16(33, 0, n * hkv * dh).reshape(n, hkv, dh)
+    v = W.normal_bf16(33, 1, n * hkv * dh).reshape(n, hkv, dh)
+    w = W.uniform_bf16(33, 2, dh, 0.5, 1.5)
+    want_k, want_v, want_lens, bad = oracle.paged_append(pk, pv, bt, lens, nsl, k_raw, v, w, ps)
+    assert not bad
+    dk, dv, dl = U.bf16_dev(pk), U.bf16_dev(pv), U.i32_dev(lens)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    D().paged_append(U.bf16_dev(k_raw), U.i32_dev(nsl), dl, U.i32_dev(bt), U.bf16_dev(w), dk, v=U.bf16_dev(v),
+                     v_pool=dv, status=status)
+    torch.cuda.synchronize()
+    assert status.item() == 0
+    assert dl.cpu().numpy().tolist() == want_lens.tolist()
+    assert np.array_equal(U.dev_bits(dv).reshape(pv.shape), want_v)
+    got_k = U.dev_bits(dk).reshape(pk.shape)
+    assert np.mean(got_k == want_k) > 0.999
