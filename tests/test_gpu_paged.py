@@ -76,7 +76,7 @@ def test_paged_matches_oracle_bf16(name, page_size, kw):
     U.assert_close_bf16(got, _oracle_paged(b, kp, vp, bt, page_size), f"{name} ps={page_size}")
 
 
-@pytest.mark.parametrize("name", ["qwen3_0p6b", "swa_small"])
+@pytest.mark.parametrize("name", ["qwen3_0p6b", "swa_small", "tiny"])
 def test_paged_matches_oracle_f32(name):
     cfg = _cfg(name)
     b = W.make_batch(cfg)
