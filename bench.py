@@ -97,12 +97,24 @@ def load_peaks() -> tuple[dict, str]:
 ATTENTION_SOURCES = ("api.cu", "attention.cu", "internal.h", "norm_rope.cuh", "ptx.cuh")
 
 
+def _code_only(text: str) -> str:
+    """The source without comments and blank lines, so that editing a comment keeps the hash."""
+    import re
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    out = []
+    for line in text.splitlines():
+        code = line.split("//", 1)[0].rstrip() if '"' not in line else line.rstrip()
+        if code.strip():
+            out.append(code)
+    return "\n".join(out)
+
+
 def kernel_source_hash() -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "speculative_decoding_draft_rmsnorm_gb300", "csrc")
     for name in ATTENTION_SOURCES:
-        with open(os.path.join(csrc, name), "rb") as f:
-            h.update(name.encode() + f.read())
+        with open(os.path.join(csrc, name), encoding="utf-8") as f:
+            h.update(name.encode() + _code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 

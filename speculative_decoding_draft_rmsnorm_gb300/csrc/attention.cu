@@ -9,11 +9,13 @@
 //
 // Three launches, chained with programmatic dependent launch:
 //   A  prologue: q^ = rope(rmsnorm(q)), k^blk = rope(rmsnorm(k_blk)) into the workspace
-//      (bf16; in precise mode also the bf16 remainders), and, in block 0, the table of
-//      groups (request, kv head, query tile) with their key-tile counts and prefix offsets.
+//      (bf16; in precise mode also the bf16 remainders), and, in its first kTableBlocks
+//      blocks, the table of groups (request, kv head, query tile) with their key-tile
+//      counts and prefix offsets, and one schedule record per attention CTA.
 //   B  attention: persistent CTAs, one per SM. Balanced (stream-K) schedule: the groups'
-//      key tiles are laid end to end and CTA c takes tiles [c*T/G, (c+1)*T/G), so every
-//      CTA streams the same number of K/V tiles whatever the raggedness; a group that
+//      key tiles are laid end to end and each CTA takes a contiguous range of equal cost
+//      (a tile, plus a little more for every group it starts; balanced_first_tile), so
+//      every CTA streams about the same work whatever the raggedness; a group that
 //      straddles CTAs is processed as segments whose partials are combined in C.
 //      Warp 0 streams Q / K / V tiles with TMA (128-byte swizzle); warp 1 issues
 //      tcgen05 MMAs: S = Q K^T into tensor memory (M = 64 query rows = G heads x block
