@@ -211,10 +211,14 @@ def paged_append(k_pool, v_pool, block_table, seq_lens, new_start_loc, k_raw, v,
     block_table[r, p // page_size]; the length then grows by count.
 
     Rows new_start_loc[r] .. new_start_loc[r+1] of k_raw / v belong to request r; rows
-    outside [new_start_loc[0], new_start_loc[N]) belong to none and are ignored. A row whose
-    page index is past the table, or whose page id is outside the pool, is not written and
-    sets the returned flag. new_start_loc must be nondecreasing, start at >= 0 and end at
-    <= len(k_raw); otherwise nothing changes and the flag is set.
+    outside [new_start_loc[0], new_start_loc[N]) belong to none and are ignored. The page
+    checks the store's capacity before it writes anything and leaves the store as it was
+    when the rows do not fit; per request the same holds here: if any new row of a request
+    would fall past its block table (page index >= max_pages) or on a page id outside the
+    pool, none of that request's rows is written, its length does not move, and the
+    returned flag is set. The other requests append as usual. new_start_loc must be
+    nondecreasing, start at >= 0 and end at <= len(k_raw); otherwise nothing changes and
+    the flag is set.
 
     Returns (k_pool, v_pool, seq_lens, flag): new arrays, the inputs are not modified.
     """
@@ -233,26 +237,34 @@ def paged_append(k_pool, v_pool, block_table, seq_lens, new_start_loc, k_raw, v,
     flag = False
     rows, dst_page, dst_off, pos = [], [], [], []
     for r in range(n_req):
-        for i in range(int(nsl[r + 1] - nsl[r])):
+        count = int(nsl[r + 1] - nsl[r])
+        if count == 0:
+            continue
+        # the request's rows and their destinations, all checked before any is written
+        mine = []
+        for i in range(count):
             p = int(lens[r]) + i
             if p < 0 or p // page_size >= max_pages:
-                flag = True
-                continue
+                break
             page = int(bt[r, p // page_size])
             if page < 0 or page >= num_pages:
-                flag = True
-                continue
-            rows.append(int(nsl[r]) + i)
+                break
+            mine.append((int(nsl[r]) + i, page, p % page_size, p))
+        if len(mine) < count:
+            flag = True
+            continue
+        for row, page, off, p in mine:
+            rows.append(row)
             dst_page.append(page)
-            dst_off.append(p % page_size)
+            dst_off.append(off)
             pos.append(p)
+        lens[r] += count
     if rows:
         k16 = context_kv(k_raw[rows], np.array(pos, dtype=np.int32), k_norm_w, eps, theta)[1]
         for j, (pg, off) in enumerate(zip(dst_page, dst_off)):
             kp[pg, off] = k16[j]
             if v is not None:
                 vp[pg, off] = v[rows[j]]
-    lens += np.diff(nsl)
     return kp, vp, lens.astype(np.int32), flag
 
 

@@ -74,15 +74,38 @@ def test_appending_in_two_steps_equals_one_step():
     assert not (one[3] or a[3] or b[3])
 
 
-def test_rows_past_the_table_or_pool_are_flagged_and_not_written():
+def test_a_request_that_does_not_fit_changes_nothing():
+    # the page's capacity check comes before any write: a request whose new rows run past its
+    # block table, or onto a page id outside the pool, writes none of them and keeps its length
     k, v, w = _rows(6)
-    # request 0 has a 2-page table (4 rows of 2) and holds 3: rows at positions 3 fits, 4 and 5 do not
+    # a 2-page table (4 rows of 2) holding 3 rows: position 3 would fit, 4 and 5 do not
     kp, vp, lens, bad = oracle.paged_append(_pool(4, 2), _pool(4, 2), [[0, 1]], [3], [0, 3], k[:3], v[:3], w, 2)
-    assert bad and lens.tolist() == [6]
-    assert np.array_equal(vp[1, 1], v[0]) and np.all(vp[:1] == FILL) and np.all(vp[2:] == FILL)
-    # a page id outside the pool
-    kp, vp, lens, bad = oracle.paged_append(_pool(4, 2), _pool(4, 2), [[9, 1]], [0], [0, 2], k[:2], v[:2], w, 2)
-    assert bad and np.all(vp == FILL)
+    assert bad and lens.tolist() == [3]
+    assert np.all(vp == FILL) and np.all(kp == FILL)
+    # exactly full: positions 3 only
+    kp, vp, lens, bad = oracle.paged_append(_pool(4, 2), _pool(4, 2), [[0, 1]], [3], [0, 1], k[:1], v[:1], w, 2)
+    assert not bad and lens.tolist() == [4] and np.array_equal(vp[1, 1], v[0])
+    # a page id outside the pool on the second page only: the first page's row is not written either
+    kp, vp, lens, bad = oracle.paged_append(_pool(4, 2), _pool(4, 2), [[2, 9]], [1], [0, 2], k[:2], v[:2], w, 2)
+    assert bad and lens.tolist() == [1] and np.all(vp == FILL)
     # start locations that run past the rows: nothing happens
     kp, vp, lens, bad = oracle.paged_append(_pool(4, 2), _pool(4, 2), [[0, 1]], [0], [0, 7], k, v, w, 2)
     assert bad and lens.tolist() == [0] and np.all(vp == FILL)
+
+
+def test_the_requests_that_fit_append_as_if_alone():
+    # request 1 overflows its 2-page table; requests 0 and 2 must come out as an append of
+    # just their rows, and request 1's pages and length stay as they were
+    ps = 4
+    k, v, w = _rows(17)
+    bt = [[0, 1], [2, 3], [4, 5]]
+    lens = [1, 5, 0]
+    nsl = [0, 6, 10, 17]  # request 1 appends 4 rows after 5: positions 5..8, past 8 rows
+    kp, vp, out_lens, bad = oracle.paged_append(_pool(6, ps), _pool(6, ps), bt, lens, nsl, k, v, w, ps)
+    assert bad and out_lens.tolist() == [7, 5, 7]
+    idx = list(range(0, 6)) + list(range(10, 17))
+    alone = oracle.paged_append(_pool(6, ps), _pool(6, ps), [[0, 1], [4, 5]], [1, 0], [0, 6, 13], k[idx], v[idx], w,
+                                ps)
+    assert not alone[3]
+    assert np.array_equal(kp, alone[0]) and np.array_equal(vp, alone[1])
+    assert np.all(vp[2:4] == FILL) and np.all(kp[2:4] == FILL)
