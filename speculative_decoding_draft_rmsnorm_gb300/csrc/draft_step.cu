@@ -14,6 +14,7 @@
 
 #include "../../include/dflash.h"
 #include "internal.h"
+#include "norm_rope.cuh"
 #include "ptx.cuh"
 
 namespace dflash {
@@ -46,22 +47,31 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 // ------------------------------------------------------------------ paged append: lengths
 // Runs after the row kernel (programmatic launch: it waits for that grid to finish before it
 // reads or writes anything), so every row saw the old lengths. One block: the start
-// locations are checked first, and the lengths move only if all of them are consistent.
-__global__ void __launch_bounds__(1024) append_lengths_kernel(const int32_t* new_start_loc, int32_t* seq_lens,
-                                                              int num_reqs, int64_t n_rows, uint32_t* err) {
+// locations are checked first, and the lengths move only if all of them are consistent; then
+// every request whose whole append fits (the row kernel's own test) grows by its count, and
+// one that does not fit keeps its length and is reported.
+__global__ void __launch_bounds__(1024) append_lengths_kernel(AppendMap m, int64_t n_rows, uint32_t* err) {
   grid_dependency_wait();
   int bad = 0;
-  for (int r = threadIdx.x; r <= num_reqs; r += blockDim.x) {
-    const int32_t a = new_start_loc[r];
+  for (int r = threadIdx.x; r <= m.num_reqs; r += blockDim.x) {
+    const int32_t a = m.new_start_loc[r];
     if (r == 0 && a < 0) bad = 1;
-    if (r == num_reqs && a > n_rows) bad = 1;
-    if (r < num_reqs && new_start_loc[r + 1] < a) bad = 1;
+    if (r == m.num_reqs && a > n_rows) bad = 1;
+    if (r < m.num_reqs && m.new_start_loc[r + 1] < a) bad = 1;
   }
   if (__syncthreads_or(bad)) {
     if (threadIdx.x == 0 && err) atomicOr(err, kErrMetadata);
     return;
   }
-  for (int r = threadIdx.x; r < num_reqs; r += blockDim.x) seq_lens[r] += new_start_loc[r + 1] - new_start_loc[r];
+  int overflow = 0;
+  int32_t* lens = const_cast<int32_t*>(m.seq_lens);
+  for (int r = threadIdx.x; r < m.num_reqs; r += blockDim.x) {
+    if (append_fits(m, r, 0, 1))
+      lens[r] += m.new_start_loc[r + 1] - m.new_start_loc[r];
+    else
+      overflow = 1;
+  }
+  if (__syncthreads_or(overflow) && threadIdx.x == 0 && err) atomicOr(err, kErrMetadata);
 }
 
 // ------------------------------------------------------------------ input preparation
@@ -258,7 +268,8 @@ int dflash_paged_append(const dflash_bf16* k_raw, const dflash_bf16* v, const in
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, append_lengths_kernel, new_start_loc, seq_lens, num_reqs, n, err);
+  AppendMap map{new_start_loc, seq_lens, block_table, num_reqs, max_pages_per_req, page_size, num_pages};
+  cudaError_t e = cudaLaunchKernelEx(&cfg, append_lengths_kernel, map, n, err);
   if (e != cudaSuccess) return failf(DFLASH_ERR_CUDA, "append lengths launch: %s", cudaGetErrorString(e));
   return report_error(DFLASH_OK, "");
 }

@@ -40,8 +40,32 @@ __device__ __forceinline__ float rope_turns(int pos, float hi, float lo) {
   return t - rintf(t);
 }
 
-// Row t of a paged append: 1 = mapped to (pos, dst); 0 = in no request (ignored); -1 = past
-// the request's block table or outside the pool (reported, not written).
+// Whether request r's whole append fits: positions [L, L + count) with L = seq_lens[r] all
+// fall inside its block table on page ids inside the pool. The page checks its store's
+// capacity before it writes any row (qwen3_dflash.cpp, AppendContextKVDevice), so a request
+// that does not fit writes nothing and keeps its length. `lane` / `lanes` split the page
+// checks over the lanes of a warp (lanes = 32, every lane calls with its own lane; the
+// result is the same on all of them) or run them in one thread (lane = 0, lanes = 1).
+__device__ __forceinline__ bool append_fits(const AppendMap& m, int r, int lane, int lanes) {
+  const int64_t L = m.seq_lens[r];
+  const int64_t count = static_cast<int64_t>(m.new_start_loc[r + 1]) - m.new_start_loc[r];
+  if (count <= 0) return true;
+  const int64_t last = L + count - 1;
+  if (L < 0 || last > 0x7fffffff || last / m.page_size >= m.max_pages) return false;
+  bool ok = true;
+  const int64_t p0 = L / m.page_size, p1 = last / m.page_size;
+  const int32_t* row = m.block_table + static_cast<int64_t>(r) * m.max_pages;
+  for (int64_t pg = p0 + lane; pg <= p1; pg += lanes) {
+    const int id = row[pg];
+    if (id < 0 || id >= m.num_pages) ok = false;
+  }
+  if (lanes > 1) ok = __all_sync(0xffffffffu, ok);
+  return ok;
+}
+
+// Row t of a paged append (called by all lanes of a warp with the same t): 1 = mapped to
+// (pos, dst); 0 = in no request (ignored); -1 = its request's append does not fit (reported,
+// none of the request's rows is written).
 __device__ __forceinline__ int append_row(const AppendMap& m, int64_t t, int* pos, int64_t* dst) {
   int lo = 0, hi = m.num_reqs + 1;  // first i with new_start_loc[i] > t
   while (lo < hi) {
@@ -50,10 +74,9 @@ __device__ __forceinline__ int append_row(const AppendMap& m, int64_t t, int* po
   }
   const int r = lo - 1;
   if (r < 0 || r >= m.num_reqs) return 0;
+  if (!append_fits(m, r, threadIdx.x & 31, 32)) return -1;
   const int64_t p = static_cast<int64_t>(m.seq_lens[r]) + (t - m.new_start_loc[r]);
-  if (p < 0 || p / m.page_size >= m.max_pages || p > 0x7fffffff) return -1;
   const int page = m.block_table[static_cast<int64_t>(r) * m.max_pages + p / m.page_size];
-  if (page < 0 || page >= m.num_pages) return -1;
   *pos = static_cast<int>(p);
   *dst = static_cast<int64_t>(page) * m.page_size + p % m.page_size;
   return 1;
