@@ -78,6 +78,10 @@ DFLASH_API const char* dflash_last_error(void);
 /* Library ABI version: (major << 16) | minor. */
 DFLASH_API int dflash_version(void);
 
+/* Bit that dflash_context_kv, dflash_paged_append and dflash_prepare_inputs OR into their
+ * `status` word. */
+enum { DFLASH_STATUS_METADATA = 2 /* a device index or length was out of range; see the call */ };
+
 /*
  * dflash_context_kv -- write rows into the draft model's context K/V store.
  * (qwen3_dflash.cpp, PrecomputeContextKVDevice: k_norm over head_dim, then RopeNeox at
@@ -89,18 +93,20 @@ DFLASH_API int dflash_version(void);
  *   k_norm_w bf16 [Dh]          k_norm weight
  *   slot     int32 [n] or NULL  destination row of each new row in the store; NULL means
  *                               row i goes to row i. Slots must be distinct and in
- *                               [0, capacity); a row whose slot is out of range is skipped
- *                               (checked on device, not reported).
+ *                               [0, capacity); a row whose slot is out of range is not
+ *                               written (checked on device) and reported through status.
  *   ctx_k    bf16 [capacity, Hkv, Dh] store K: out[slot[i]] = rope(rmsnorm(k_raw[i]))
  *   ctx_v    bf16 [capacity, Hkv, Dh] store V: out[slot[i]] = v[i] (ignored if v is NULL)
  *   eps, rope_theta             RMSNorm epsilon, RoPE base (inv_freq_i = theta^(-2i/Dh))
+ *   status   int32 device word or NULL: the call ORs DFLASH_STATUS_METADATA into it when a
+ *                               row's slot is outside [0, capacity); it never clears it
  *   Dh in {64, 128}; Hkv >= 1. k_raw may alias ctx_k (and v ctx_v) when slot is NULL.
  *   Math: f32 RMSNorm and rotation with an exactly reduced angle; one bf16 rounding.
  */
 DFLASH_API int dflash_context_kv(const dflash_bf16* k_raw, const dflash_bf16* v, const int32_t* ctx_pos,
                       const dflash_bf16* k_norm_w, const int32_t* slot, int64_t n, int hkv, int dh,
                       float eps, float rope_theta, dflash_bf16* ctx_k, dflash_bf16* ctx_v,
-                      int64_t capacity, dflash_stream_t stream);
+                      int64_t capacity, int32_t* status, dflash_stream_t stream);
 
 /*
  * Bytes of device workspace dflash_block_attention needs on the current device for these
@@ -217,8 +223,10 @@ DFLASH_API int dflash_block_attention_paged(const dflash_bf16* q_raw, const dfla
  * nothing. The first call on a device looks up the array's device address with that
  * device current and caches it; make that first call before any stream capture. All
  * calls on a device share the array, so calls that overlap on the GPU (two streams at
- * once) race and must not be issued. dflash_check_error cannot read this scratch; errors
- * of the call itself are returned and described by dflash_last_error.
+ * once) race and must not be issued. Errors found from the host arguments are returned
+ * and described by dflash_last_error; errors only the device can see (bad device metadata,
+ * a bounded wait that ran out) are recorded in the built-in scratch and read with
+ * dflash_block_attention_noalloc_check_error.
  */
 DFLASH_API int dflash_block_attention_noalloc(const dflash_bf16* q_raw, const dflash_bf16* k_blk,
                                               const dflash_bf16* v_blk, const dflash_bf16* ctx_k,
@@ -230,8 +238,14 @@ DFLASH_API int dflash_block_attention_noalloc(const dflash_bf16* q_raw, const df
                                               float eps, float rope_theta, float scale, int causal, int window,
                                               int out_dtype, void* out, int flags, dflash_stream_t stream);
 
-/* Bit that dflash_paged_append and dflash_prepare_inputs OR into their `status` word. */
-enum { DFLASH_STATUS_METADATA = 2 /* a device index or length was out of range; see the call */ };
+/*
+ * dflash_block_attention_noalloc_check_error -- dflash_check_error for the built-in scratch
+ * of the current device: reads the device error word the last noalloc call on this device
+ * left there (waits for `stream`). Returns DFLASH_OK, DFLASH_ERR_DEVICE_TIMEOUT or
+ * DFLASH_ERR_DEVICE_METADATA; DFLASH_ERR_INVALID_ARG if no noalloc call has run on the
+ * device. Allocates nothing.
+ */
+DFLASH_API int dflash_block_attention_noalloc_check_error(dflash_stream_t stream);
 
 /*
  * dflash_paged_append -- append new context rows to a paged context K/V store and advance
@@ -256,10 +270,12 @@ enum { DFLASH_STATUS_METADATA = 2 /* a device index or length was out of range; 
  *                                     block_table[r, p / page_size]
  *   eps, rope_theta                   as dflash_context_kv (same kernel arithmetic)
  *   status         int32 device word or NULL. The call ORs DFLASH_STATUS_METADATA into it
- *                  when a row's page index is past the table or its page id outside the
- *                  pool (that row is not written; the length still grows), or when
- *                  new_start_loc is not nondecreasing within [0, n] (then no length moves).
- *                  The call never clears it.
+ *                  when a request's append does not fit -- one of its new rows would fall
+ *                  past its block table or on a page id outside the pool: like the page's
+ *                  capacity check, which comes before any write, none of that request's
+ *                  rows is written and its length stays; the other requests append -- or
+ *                  when new_start_loc is not nondecreasing within [0, n] (then no length
+ *                  moves). The call never clears it.
  *   Dh in {64, 128}; any page_size >= 1. Two launches: the rows, then the lengths (which
  *   waits for the rows, so every row sees the old length). Allocates nothing.
  */

@@ -26,7 +26,7 @@ __all__ = ["load", "lib_path", "context_kv", "paged_append", "prepare_inputs", "
            "ERR_DEVICE_METADATA"]
 
 OUT_BF16, OUT_F32 = 0, 1
-STATUS_METADATA = 2  # bit ORed into the status word of paged_append / prepare_inputs
+STATUS_METADATA = 2  # bit ORed into the status word of context_kv / paged_append / prepare_inputs
 FLAG_FORCE_SPLIT, FLAG_NO_SPLIT = 1, 2
 ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_WORKSPACE, ERR_CUDA, ERR_DEVICE_TIMEOUT, ERR_DEVICE_METADATA = \
     -1, -2, -3, -4, -5, -6
@@ -64,7 +64,7 @@ def load(build_if_missing: bool = True):
         lib.dflash_version.restype = I32
         lib.dflash_version.argtypes = []
         lib.dflash_context_kv.restype = I32
-        lib.dflash_context_kv.argtypes = [P, P, P, P, P, I64, I32, I32, F32, F32, P, P, I64, P]
+        lib.dflash_context_kv.argtypes = [P, P, P, P, P, I64, I32, I32, F32, F32, P, P, I64, P, P]
         lib.dflash_block_attention_workspace_size.restype = SZ
         lib.dflash_block_attention_workspace_size.argtypes = [I32, I64, I32, I32, I32, I64, I32, I32, I32, I32, I32, I32]
         lib.dflash_block_attention.restype = I32
@@ -119,9 +119,12 @@ def _check_tensor(name, t, dtype, shape=None):
         raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
 
 
-def context_kv(k_raw, ctx_pos, k_norm_w, ctx_k, *, v=None, ctx_v=None, slot=None, eps=1e-6, theta=1e6,
-               stream=None) -> None:
-    """Writes rope(rmsnorm(k_raw)) into ctx_k (and v into ctx_v) at rows `slot` (or 0..n-1)."""
+def context_kv(k_raw, ctx_pos, k_norm_w, ctx_k, *, v=None, ctx_v=None, slot=None, status=None, eps=1e-6,
+               theta=1e6, stream=None) -> None:
+    """Writes rope(rmsnorm(k_raw)) into ctx_k (and v into ctx_v) at rows `slot` (or 0..n-1).
+
+    status: an optional int32 device word that receives STATUS_METADATA when a slot is out of
+    range (that row is not written)."""
     import torch
     n, hkv, dh = k_raw.shape
     _check_tensor("k_raw", k_raw, torch.bfloat16)
@@ -131,10 +134,12 @@ def context_kv(k_raw, ctx_pos, k_norm_w, ctx_k, *, v=None, ctx_v=None, slot=None
     _check_tensor("slot", slot, torch.int32, (n,))
     _check_tensor("ctx_k", ctx_k, torch.bfloat16)
     _check_tensor("ctx_v", ctx_v, torch.bfloat16, None if ctx_v is None else tuple(ctx_k.shape))
+    _check_tensor("status", status, torch.int32, (1,))
     if tuple(ctx_k.shape[1:]) != (hkv, dh):
         raise ValueError("ctx_k must be [capacity, Hkv, Dh]")
     rc = load().dflash_context_kv(_ptr(k_raw), _ptr(v), _ptr(ctx_pos), _ptr(k_norm_w), _ptr(slot), n, hkv, dh,
-                                  float(eps), float(theta), _ptr(ctx_k), _ptr(ctx_v), ctx_k.shape[0], _stream(stream))
+                                  float(eps), float(theta), _ptr(ctx_k), _ptr(ctx_v), ctx_k.shape[0], _ptr(status),
+                                  _stream(stream))
     _raise(rc)
 
 

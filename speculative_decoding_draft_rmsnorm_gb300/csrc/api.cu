@@ -92,7 +92,7 @@ int dflash_version(void) { return (1 << 16) | 0; }
 int dflash_context_kv(const dflash_bf16* k_raw, const dflash_bf16* v, const int32_t* ctx_pos,
                       const dflash_bf16* k_norm_w, const int32_t* slot, int64_t n, int hkv, int dh, float eps,
                       float rope_theta, dflash_bf16* ctx_k, dflash_bf16* ctx_v, int64_t capacity,
-                      dflash_stream_t stream) {
+                      int32_t* status, dflash_stream_t stream) {
   if (dh != 64 && dh != 128) return fail(DFLASH_ERR_UNSUPPORTED, "head_dim %d: only 64 and 128 are implemented", dh);
   if (hkv <= 0) return fail(DFLASH_ERR_INVALID_ARG, "Hkv must be positive");
   if (n < 0 || capacity < 0) return fail(DFLASH_ERR_INVALID_ARG, "negative row count");
@@ -119,7 +119,7 @@ int dflash_context_kv(const dflash_bf16* k_raw, const dflash_bf16* v, const int3
   job.slot = slot;
   job.capacity = capacity;
   job.eps = eps;
-  job.err = nullptr;
+  job.err = reinterpret_cast<uint32_t*>(status);
   dflash::make_rope_turns(dh, static_cast<double>(rope_theta), &job.turns);
   cudaError_t e = dflash::launch_norm_rope(job, dh, sms, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail(DFLASH_ERR_CUDA, "norm_rope launch: %s", cudaGetErrorString(e));

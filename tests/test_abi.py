@@ -68,11 +68,11 @@ def test_attention_rejects_bad_host_arguments(over, code):
 def test_context_kv_rejects_bad_host_arguments():
     lib = D.load()
     fake = ctypes.c_void_p(256)
-    assert lib.dflash_context_kv(fake, None, fake, fake, None, 10, 2, 96, 1e-6, 1e6, fake, None, 10, None) == \
+    assert lib.dflash_context_kv(fake, None, fake, fake, None, 10, 2, 96, 1e-6, 1e6, fake, None, 10, None, None) == \
         D.ERR_UNSUPPORTED
-    assert lib.dflash_context_kv(fake, None, fake, fake, None, 11, 2, 64, 1e-6, 1e6, fake, None, 10, None) == \
+    assert lib.dflash_context_kv(fake, None, fake, fake, None, 11, 2, 64, 1e-6, 1e6, fake, None, 10, None, None) == \
         D.ERR_INVALID_ARG
-    assert lib.dflash_context_kv(fake, None, fake, fake, None, 0, 2, 64, 1e-6, 1e6, fake, None, 10, None) == 0
+    assert lib.dflash_context_kv(fake, None, fake, fake, None, 0, 2, 64, 1e-6, 1e6, fake, None, 10, None, None) == 0
 
 
 def test_header_declares_the_draft_step_entry_points():
