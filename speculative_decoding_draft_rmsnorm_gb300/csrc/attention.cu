@@ -189,8 +189,11 @@ __device__ void build_groups(const PrologueParams& p, int part, int nparts) {
       q.C = p.clen[q.r];
       q.B = q1 - q.q0;
       if ((q.r == 0 && q.q0 != 0) || (q.r == p.num_reqs - 1 && q1 != p.total_q)) s_bad_global = 1;
-      const bool ok = q.B >= 0 && q.q0 >= 0 && q1 <= p.total_q && q.c0 >= 0 && c1 >= q.c0 && c1 <= p.total_ctx &&
-                      q.C >= 0 && q.C <= c1 - q.c0 && q.C <= p.max_ctx_len && q.B <= p.max_block_len;
+      // paged: the request's capacity is its block table (page ids are checked where they are
+      // read); contiguous: its segment must lie inside the store
+      const bool seg_ok = p.paged ? true : (q.c0 >= 0 && c1 >= q.c0 && c1 <= p.total_ctx);
+      const bool ok = q.B >= 0 && q.q0 >= 0 && q1 <= p.total_q && seg_ok && q.C >= 0 && q.C <= c1 - q.c0 &&
+                      q.C <= p.max_ctx_len && q.B <= p.max_block_len;
       if (!ok) {
         if (lead) atomicOr(&p.hdr[0], kErrMetadata);
         q.B = 0;

@@ -150,3 +150,23 @@ def test_paged_rejects_unsupported_page_size_and_short_table():
         _gpu_paged(b, kp, vp, bt, max_ctx_len=bt.shape[1] * 16 + 1)
     assert e.value.code == D.ERR_INVALID_ARG
     torch.cuda.synchronize()
+
+
+def test_pool_smaller_than_the_block_table_width():
+    # a block table sized for the longest context a request may reach (64 pages of 16 rows)
+    # over a pool that holds fewer pages than that: each request's live rows fit in its pages,
+    # so every request is computed and nothing is reported
+    import torch
+    import speculative_decoding_draft_rmsnorm_gb300 as D
+    cfg = dataclasses.replace(W.CONFIGS["qwen3_0p6b"], num_reqs=3)
+    b = W.make_batch(cfg, ctx_lens=[100, 37, 0], block_lens=[16, 16, 5])
+    ck = U.stored_ctx_k(b)
+    kp, vp, bt = _paged_inputs(b, ck, 16)
+    wide = np.full((bt.shape[0], 64), -1, dtype=np.int32)  # room for 1024 rows per request
+    wide[:, :bt.shape[1]] = bt
+    assert kp.shape[0] < wide.shape[1]  # the pool has fewer pages than a table row
+    ws = D.alloc_workspace(D.workspace_size(3, b.q.shape[0], cfg.hq, cfg.hkv, cfg.dh, kp.shape[0] * 16, 1024, 16))
+    got = _gpu_paged(b, kp, vp, wide, max_ctx_len=1024, workspace=ws)
+    torch.cuda.synchronize()
+    D.check_error(ws)
+    U.assert_close_bf16(U.dev_to_f64(got), _oracle_paged(b, kp, vp, wide, 16), "pool narrower than the table")
