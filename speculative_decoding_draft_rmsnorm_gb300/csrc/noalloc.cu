@@ -30,9 +30,11 @@ static __device__ __align__(256) unsigned char g_scratch[kScratchBytes];
 
 namespace {
 
+constexpr int kMaxDevices = 64;
+
 struct ScratchCache {
   std::mutex mu;
-  void* ptr[64] = {};
+  void* ptr[kMaxDevices] = {};
 };
 
 ScratchCache& cache() {
@@ -63,9 +65,14 @@ DFLASH_API int dflash_block_attention_noalloc(
   }
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess || dev < 0 || dev >= 64) {
+  if (e != cudaSuccess) {
     std::snprintf(msg, sizeof msg, "cudaGetDevice: %s", cudaGetErrorString(e));
     return dflash::report_error(DFLASH_ERR_CUDA, msg);
+  }
+  if (dev < 0 || dev >= kMaxDevices) {
+    std::snprintf(msg, sizeof msg, "device %d: the built-in scratch serves devices 0 to %d only", dev,
+                  kMaxDevices - 1);
+    return dflash::report_error(DFLASH_ERR_UNSUPPORTED, msg);
   }
   void* scratch = nullptr;
   {
@@ -84,6 +91,29 @@ DFLASH_API int dflash_block_attention_noalloc(
                                 positions, q_norm_w, k_norm_w, num_reqs, total_q, hq, hkv, dh, total_ctx, max_ctx_len,
                                 max_block_len, eps, rope_theta, scale, causal, window, out_dtype, out, scratch,
                                 kScratchBytes, flags, stream);
+}
+
+// The device error word of the last noalloc call on the current device lives in the built-in
+// scratch, which the caller has no pointer to; this reads it exactly as dflash_check_error
+// reads a caller's workspace (it waits for `stream`).
+DFLASH_API int dflash_block_attention_noalloc_check_error(dflash_stream_t stream) {
+  char msg[160];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) {
+    std::snprintf(msg, sizeof msg, "cudaGetDevice: %s", cudaGetErrorString(e));
+    return dflash::report_error(DFLASH_ERR_CUDA, msg);
+  }
+  void* scratch = nullptr;
+  if (dev >= 0 && dev < kMaxDevices) {
+    std::lock_guard<std::mutex> lock(cache().mu);
+    scratch = cache().ptr[dev];
+  }
+  if (!scratch) {
+    std::snprintf(msg, sizeof msg, "no dflash_block_attention_noalloc call has run on device %d", dev);
+    return dflash::report_error(DFLASH_ERR_INVALID_ARG, msg);
+  }
+  return dflash_check_error(scratch, stream);
 }
 
 }  // extern "C"
