@@ -377,9 +377,9 @@ struct Layout {
   // barrier indices
   static constexpr int K_FULL = 0, K_EMPTY = NK, V_FULL = 2 * NK, V_EMPTY = 2 * NK + NV;
   static constexpr int Q_FULL = 2 * NK + 2 * NV, Q_EMPTY = Q_FULL + 2, S_FULL = Q_FULL + 4, S_EMPTY = Q_FULL + 6;
-  static constexpr int P_FULL = Q_FULL + 8, P_EMPTY = Q_FULL + 10, O_FULL = Q_FULL + 12, O_EMPTY = Q_FULL + 13;
-  static constexpr int DRAIN = Q_FULL + 14;  // final commit of the MMA thread (its own barrier)
-  static constexpr int NBARS = Q_FULL + 15;
+  static constexpr int P_FULL = Q_FULL + 8, P_EMPTY = Q_FULL + 10, O_FULL = Q_FULL + 12, O_EMPTY = Q_FULL + 14;
+  static constexpr int DRAIN = Q_FULL + 16;  // final commit of the MMA thread (its own barrier)
+  static constexpr int NBARS = Q_FULL + 17;
   static constexpr int OFF_MISC = OFF_BAR + NBARS * 8;
   static constexpr int OFF_REC = (OFF_MISC + 64 + 15) / 16 * 16;  // CtaRecord (80 bytes)
   static constexpr int BYTES = OFF_REC + 80;
@@ -472,6 +472,11 @@ struct SegIter {
     g += gridDim.x;
     return true;
   }
+  // Starts loading the descriptor the next call of next() reads (a segment switch then finds
+  // it in L1 instead of waiting on L2 behind the K/V stream).
+  __device__ void prefetch_next() const {
+    if (g < ng) prefetch_l1(groups + g);
+  }
 };
 
 // Producer of the paged instantiation (the whole warp 0). Q and block tiles come by TMA from
@@ -501,6 +506,7 @@ __device__ __forceinline__ void produce_paged(const AttnParams& p, const CUtenso
   bool ok = true;
   Seg sg;
   for (; ok && it.next(sg); ++iu) {
+    if (lane == 0) it.prefetch_next();
     const Group& U = sg.grp;
     const int qb = iu % NQ;
     if (!(ok = wait0(bar(L::Q_EMPTY + qb), ((iu / NQ) & 1) ^ 1))) break;
@@ -627,8 +633,10 @@ attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
       mbar_init(bar(L::P_FULL + i), 4);
       mbar_init(bar(L::P_EMPTY + i), 1);
     }
-    mbar_init(bar(L::O_FULL), 1);
-    mbar_init(bar(L::O_EMPTY), 4);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bar(L::O_FULL + i), 1);
+      mbar_init(bar(L::O_EMPTY + i), 4);
+    }
     mbar_init(bar(L::DRAIN), 1);
     *abort_flag = 0;
     mbar_fence_init();
@@ -688,6 +696,7 @@ attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
       SegIter it = make_iter();
       Seg sg;
       for (; ok && it.next(sg); ++iu) {
+        it.prefetch_next();
         const Group& U = sg.grp;
         const int qb = iu % NQ;
         if (!(ok = mbar_wait(bar(L::Q_EMPTY + qb), ((iu / NQ) & 1) ^ 1, abort_flag))) break;
@@ -768,78 +777,102 @@ attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
+    // One pass over the CTA's tiles, segment after segment: S = Q K^T of the next tile is issued
+    // before O += P V of the current one, across segment boundaries too (with two Q buffers),
+    // so the next segment's first scores do not wait for the last V of this one. Segment iu
+    // accumulates into O buffer iu & 1, so its first PV waits only for the epilogue of
+    // segment iu - 2.
     if (lane == 0) {
-      uint32_t gk = 0, gv = 0, gj = 0;
-      int iu = 0;
+      uint32_t gk = 0, gv = 0, gq = 0, gp = 0;  // K / V tiles consumed, QK / PV tiles issued
       bool ok = true;
       const uint32_t idesc_pv = umma_idesc_bf16(kTileRows, DH, 0, 1);
       SegIter it = make_iter();
-      Seg sg;
-      for (; ok && it.next(sg); ++iu) {
+      Seg cur, nxt;  // segment iu and, once fetched, segment iu + 1
+      bool have_nxt = false;
+      // S = Q K^T of tile j of segment iu (sg)
+      auto issue_qk = [&](const Seg& sg, int iu, int j) -> bool {
         const Group& U = sg.grp;
         const int qb = iu % NQ;
-        const int n = sg.t1 - sg.t0;
-        if (!(ok = mbar_wait(bar(L::Q_FULL + qb), (iu / NQ) & 1, abort_flag))) break;
-        tc_fence_after();
+        if (j == 0) {
+          if (!mbar_wait(bar(L::Q_FULL + qb), (iu / NQ) & 1, abort_flag)) return false;
+        }
         const uint32_t q_addr = sbase + L::OFF_Q + qb * L::QBT;
-        auto issue_qk = [&](int j) -> bool {
-          const uint32_t g = gj + j;
-          const int sb = g & 1;
-          const int slot = static_cast<int>(gk % NK);
-          if (!mbar_wait(bar(L::K_FULL + slot), (gk / NK) & 1, abort_flag)) return false;
-          if (!mbar_wait(bar(L::S_EMPTY + sb), ((g >> 1) & 1) ^ 1, abort_flag)) return false;
-          tc_fence_after();
-          const TileInfo ti = tile_info(U, sg.t0 + j, p.blk_tile);
-          const int nq = min(kTileKeys, (ti.valid + 15) & ~15);
-          const uint32_t idesc = umma_idesc_bf16(kTileRows, nq, 0, 0);
-          const uint32_t k_addr = sbase + L::OFF_K + slot * L::KB;
+        const int sb = gq & 1;
+        const int slot = static_cast<int>(gk % NK);
+        if (!mbar_wait(bar(L::K_FULL + slot), (gk / NK) & 1, abort_flag)) return false;
+        if (!mbar_wait(bar(L::S_EMPTY + sb), ((gq >> 1) & 1) ^ 1, abort_flag)) return false;
+        tc_fence_after();
+        const TileInfo ti = tile_info(U, sg.t0 + j, p.blk_tile);
+        const int nq = min(kTileKeys, (ti.valid + 15) & ~15);
+        const uint32_t idesc = umma_idesc_bf16(kTileRows, nq, 0, 0);
+        const uint32_t k_addr = sbase + L::OFF_K + slot * L::KB;
 #pragma unroll
-          for (int kk = 0; kk < DH / 16; ++kk) {
-            const uint32_t qo = (kk >> 2) * (kTileRows * 128) + (kk & 3) * 32;
-            const uint32_t ko = (kk >> 2) * (kTileKeys * 128) + (kk & 3) * 32;
-            const uint64_t b = umma_desc_sw128(k_addr + ko, 16, 1024);
-            umma_bf16_ss(tmem + sb * 128, umma_desc_sw128(q_addr + qo, 16, 1024), b, idesc, kk > 0 ? 1u : 0u);
-            if (PRECISE) {
-              // S = Q_hi K + Q_lo K (+ Q_hi K_lo on block tiles, whose keys are rounded here)
-              umma_bf16_ss(tmem + sb * 128, umma_desc_sw128(q_addr + L::QB + qo, 16, 1024), b, idesc, 1u);
-              if (ti.blk)
-                umma_bf16_ss(tmem + sb * 128, umma_desc_sw128(q_addr + qo, 16, 1024),
-                             umma_desc_sw128(k_addr + ko + 64 * 128, 16, 1024), idesc, 1u);
-            }
+        for (int kk = 0; kk < DH / 16; ++kk) {
+          const uint32_t qo = (kk >> 2) * (kTileRows * 128) + (kk & 3) * 32;
+          const uint32_t ko = (kk >> 2) * (kTileKeys * 128) + (kk & 3) * 32;
+          const uint64_t b = umma_desc_sw128(k_addr + ko, 16, 1024);
+          umma_bf16_ss(tmem + sb * 128, umma_desc_sw128(q_addr + qo, 16, 1024), b, idesc, kk > 0 ? 1u : 0u);
+          if (PRECISE) {
+            // S = Q_hi K + Q_lo K (+ Q_hi K_lo on block tiles, whose keys are rounded here)
+            umma_bf16_ss(tmem + sb * 128, umma_desc_sw128(q_addr + L::QB + qo, 16, 1024), b, idesc, 1u);
+            if (ti.blk)
+              umma_bf16_ss(tmem + sb * 128, umma_desc_sw128(q_addr + qo, 16, 1024),
+                           umma_desc_sw128(k_addr + ko + 64 * 128, 16, 1024), idesc, 1u);
           }
-          umma_commit(bar(L::S_FULL + sb));
-          umma_commit(bar(L::K_EMPTY + slot));
-          if (j == n - 1) umma_commit(bar(L::Q_EMPTY + qb));
-          ++gk;
-          return true;
-        };
-        if (!(ok = issue_qk(0))) break;
+        }
+        umma_commit(bar(L::S_FULL + sb));
+        umma_commit(bar(L::K_EMPTY + slot));
+        if (j == sg.t1 - sg.t0 - 1) umma_commit(bar(L::Q_EMPTY + qb));
+        ++gk;
+        ++gq;
+        return true;
+      };
+      bool have_cur = it.next(cur);
+      if (have_cur) ok = issue_qk(cur, 0, 0);
+      for (int iu = 0; ok && have_cur; ++iu) {
+        const Seg& sg = cur;
+        const int n = sg.t1 - sg.t0;
+        const uint32_t o_col = 256 + static_cast<uint32_t>((iu & 1) * DH);
+        bool next_issued = false;
+        it.prefetch_next();
         for (int j = 0; j < n && ok; ++j) {
-          if (j + 1 < n && !(ok = issue_qk(j + 1))) break;
-          const uint32_t g = gj + j;
-          const int pb = g & 1;
+          if (j + 1 < n) {
+            if (!(ok = issue_qk(sg, iu, j + 1))) break;
+          } else if (NQ > 1 && (have_nxt = it.next(nxt))) {
+            // the next segment's first QK before this segment's last PV
+            if (!(ok = issue_qk(nxt, iu + 1, 0))) break;
+            next_issued = true;
+          }
+          const int pb = gp & 1;
           const int vslot = static_cast<int>(gv % NV);
-          if (!(ok = mbar_wait(bar(L::P_FULL + pb), (g >> 1) & 1, abort_flag))) break;
+          if (!(ok = mbar_wait(bar(L::P_FULL + pb), (gp >> 1) & 1, abort_flag))) break;
           if (!(ok = mbar_wait(bar(L::V_FULL + vslot), (gv / NV) & 1, abort_flag))) break;
-          if (j == 0 && !(ok = mbar_wait(bar(L::O_EMPTY), (iu & 1) ^ 1, abort_flag))) break;
+          if (j == 0 && !(ok = mbar_wait(bar(L::O_EMPTY + (iu & 1)), ((iu >> 1) & 1) ^ 1, abort_flag))) break;
           tc_fence_after();
-          const TileInfo ti = tile_info(U, sg.t0 + j, p.blk_tile);
+          const TileInfo ti = tile_info(sg.grp, sg.t0 + j, p.blk_tile);
           const int ksteps = (ti.valid + 15) >> 4;
           const uint32_t p_addr = sbase + L::OFF_P + pb * L::PBT;
           const uint32_t v_addr = sbase + L::OFF_V + vslot * L::KB;
           for (int kk = 0; kk < ksteps; ++kk) {
             const uint32_t po = (kk >> 2) * (kTileRows * 128) + (kk & 3) * 32;
             const uint64_t b = umma_desc_sw128(v_addr + kk * (16 * 128), kTileKeys * 128, 1024);
-            umma_bf16_ss(tmem + 256, umma_desc_sw128(p_addr + po, 16, 1024), b, idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
-            if (PRECISE) umma_bf16_ss(tmem + 256, umma_desc_sw128(p_addr + L::PB + po, 16, 1024), b, idesc_pv, 1u);
+            umma_bf16_ss(tmem + o_col, umma_desc_sw128(p_addr + po, 16, 1024), b, idesc_pv,
+                         (j > 0 || kk > 0) ? 1u : 0u);
+            if (PRECISE) umma_bf16_ss(tmem + o_col, umma_desc_sw128(p_addr + L::PB + po, 16, 1024), b, idesc_pv, 1u);
           }
           umma_commit(bar(L::V_EMPTY + vslot));
           umma_commit(bar(L::P_EMPTY + pb));
           ++gv;
+          ++gp;
         }
         if (!ok) break;
-        umma_commit(bar(L::O_FULL));
-        gj += n;
+        umma_commit(bar(L::O_FULL + (iu & 1)));
+        // one Q buffer: the next segment's Q is loaded after this segment's last QK, so its
+        // first QK comes after the last PV
+        if (NQ == 1) have_nxt = it.next(nxt);
+        if (!next_issued && have_nxt) ok = issue_qk(nxt, iu + 1, 0);
+        have_cur = have_nxt;
+        if (have_cur) cur = nxt;
       }
       if (!ok) atomicOr(&p.hdr[0], kErrTimeout);
       // let every issued MMA finish before the CTA releases tensor memory
@@ -862,11 +895,83 @@ attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
       if (lane == 0) r = mbar_wait(b, parity, abort_flag) ? 1 : 0;
       return __shfl_sync(0xffffffffu, r, 0) != 0;
     };
+    // A segment's epilogue runs once the next segment's first P is written (the MMA meanwhile
+    // starts the next segment in the other O buffer), or after the last segment.
+    struct Pending {
+      int row;      // output row (token * Hq + head) of this thread (complete segment)
+      float m, l;
+      int state;    // bit 0 valid, bit 1 row ok, bit 2 complete, bits 3..: segment index
+      __device__ bool valid() const { return state & 1; }
+    } pend;
+    pend.state = 0;
+    constexpr int CH = DH / 2 / 32;  // 32-column chunks per half row of O
+    auto epilogue = [&](const Pending& e) -> bool {
+      const int e_iu = e.state >> 3;
+      if (!wait_warp(bar(L::O_FULL + (e_iu & 1)), (e_iu >> 1) & 1)) return false;
+      tc_fence_after();
+      uint32_t o[CH][32];
+      const uint32_t o_col = 256 + static_cast<uint32_t>((e_iu & 1) * DH);
+#pragma unroll
+      for (int ch = 0; ch < CH; ++ch) tmem_ld_16x32bx2_x32<DH / 2>(tmem + lane_base + o_col + ch * 32, o[ch]);
+      tmem_wait_ld();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(L::O_EMPTY + (e_iu & 1)));
+      const float l_tot = e.l + __shfl_xor_sync(0xffffffffu, e.l, 16);
+      if (!(e.state & 2)) return true;
+      if (e.state & 4) {
+        const float inv = l_tot > 0.0f ? 1.0f / l_tot : 0.0f;
+        if (p.out_f32) {
+          float* dst = reinterpret_cast<float*>(p.out) + static_cast<int64_t>(e.row) * DH + half * (DH / 2);
+#pragma unroll
+          for (int ch = 0; ch < CH; ++ch)
+#pragma unroll
+            for (int x = 0; x < 32; x += 4)
+              *reinterpret_cast<float4*>(dst + ch * 32 + x) =
+                  make_float4(__uint_as_float(o[ch][x]) * inv, __uint_as_float(o[ch][x + 1]) * inv,
+                              __uint_as_float(o[ch][x + 2]) * inv, __uint_as_float(o[ch][x + 3]) * inv);
+        } else {
+          uint16_t* dst = reinterpret_cast<uint16_t*>(p.out) + static_cast<int64_t>(e.row) * DH + half * (DH / 2);
+#pragma unroll
+          for (int ch = 0; ch < CH; ++ch)
+#pragma unroll
+            for (int x = 0; x < 32; x += 8) {
+              uint4 v;
+              v.x = pack_bf16x2(__uint_as_float(o[ch][x]) * inv, __uint_as_float(o[ch][x + 1]) * inv);
+              v.y = pack_bf16x2(__uint_as_float(o[ch][x + 2]) * inv, __uint_as_float(o[ch][x + 3]) * inv);
+              v.z = pack_bf16x2(__uint_as_float(o[ch][x + 4]) * inv, __uint_as_float(o[ch][x + 5]) * inv);
+              v.w = pack_bf16x2(__uint_as_float(o[ch][x + 6]) * inv, __uint_as_float(o[ch][x + 7]) * inv);
+              *reinterpret_cast<uint4*>(dst + ch * 32 + x) = v;
+            }
+        }
+      } else {
+        // kept in L2 for the combine pass, which reads them after the streaming
+        const uint64_t pol_keep = l2_policy_evict_last();
+        const int pslot = 2 * static_cast<int>(blockIdx.x) + (e_iu == 0 ? 0 : 1);  // first segment, or later
+        float* dst = p.part_o + (static_cast<int64_t>(pslot) * kTileRows + rho) * DH + half * (DH / 2);
+#pragma unroll
+        for (int ch = 0; ch < CH; ++ch)
+#pragma unroll
+          for (int x = 0; x < 32; x += 4)
+            st_global_v4_hint(dst + ch * 32 + x,
+                              make_float4(__uint_as_float(o[ch][x]), __uint_as_float(o[ch][x + 1]),
+                                          __uint_as_float(o[ch][x + 2]), __uint_as_float(o[ch][x + 3])),
+                              pol_keep);
+        if (half == 0)
+          st_global_v2_hint(p.part_ml + (static_cast<int64_t>(pslot) * kTileRows + rho) * 2, e.m, l_tot, pol_keep);
+      }
+      return true;
+    };
+    // One pass per segment, plus a last one without tiles for the last segment's epilogue, so
+    // that the tile body and the epilogue each appear once in the code (cold code is fetched
+    // from memory the first time it runs).
     SegIter it = make_iter();
     Seg sg;
-    for (; ok && it.next(sg); ++iu) {
+    bool have = it.next(sg);
+    for (; ok && (have || pend.valid()); ++iu) {
+      if (have && lane == 0) it.prefetch_next();
       const Group& U = sg.grp;
-      const int n = sg.t1 - sg.t0;
+      const int n = have ? sg.t1 - sg.t0 : 0;
       const bool row_ok = rho < U.rows;
       const int b = U.tok0 + rho / p.g;        // block index of this row
       const int i = U.clen + b;                // combined query index
@@ -880,7 +985,8 @@ attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         jhi = 0;
       }
       float m_used = -INFINITY, l = 0.0f;
-      for (int j = 0; j < n; ++j) {
+      for (int j = 0; j < (n > 0 ? n : 1); ++j) {
+       if (j < n) {
         const uint32_t g = gj + j;
         const int sb = g & 1;
         const TileInfo ti = tile_info(U, sg.t0 + j, p.blk_tile);
@@ -935,15 +1041,15 @@ attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
           if (!(ok = wait_warp(bar(L::P_EMPTY + ((g - 1) & 1)), ((g - 1) >> 1) & 1))) break;
           tc_fence_after();
           l *= alpha;
-          constexpr int CH = DH / 2 / 32;  // 32-column chunks per half row of O
 #pragma unroll
           for (int ch = 0; ch < CH; ++ch) {
             uint32_t o[32];
-            tmem_ld_16x32bx2_x32<DH / 2>(tmem + lane_base + 256 + ch * 32, o);
+            const uint32_t o_addr = tmem + lane_base + 256 + static_cast<uint32_t>((iu & 1) * DH) + ch * 32;
+            tmem_ld_16x32bx2_x32<DH / 2>(o_addr, o);
             tmem_wait_ld();
 #pragma unroll
             for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-            tmem_st_16x32bx2_x32<DH / 2>(tmem + lane_base + 256 + ch * 32, o);
+            tmem_st_16x32bx2_x32<DH / 2>(o_addr, o);
           }
           tmem_wait_st();
         }
@@ -1001,67 +1107,22 @@ attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(L::P_FULL + sb));
-      }
-      if (!ok) break;
-      // ---------------------------------------------------------- epilogue
-      if (!(ok = wait_warp(bar(L::O_FULL), iu & 1))) break;
-      tc_fence_after();
-      constexpr int CH = DH / 2 / 32;
-      uint32_t o[CH][32];
-#pragma unroll
-      for (int ch = 0; ch < CH; ++ch) tmem_ld_16x32bx2_x32<DH / 2>(tmem + lane_base + 256 + ch * 32, o[ch]);
-      tmem_wait_ld();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(L::O_EMPTY));
-      const float l_tot = l + __shfl_xor_sync(0xffffffffu, l, 16);
-      if (row_ok) {
-        const int gi = rho % p.g;
-        const int64_t tok = U.qsl + b;
-        const int head = U.kvh * p.g + gi;
-        if (sg.complete) {
-          const float inv = l_tot > 0.0f ? 1.0f / l_tot : 0.0f;
-          if (p.out_f32) {
-            float* dst = reinterpret_cast<float*>(p.out) + (tok * p.hq + head) * DH + half * (DH / 2);
-#pragma unroll
-            for (int ch = 0; ch < CH; ++ch)
-#pragma unroll
-              for (int e = 0; e < 32; e += 4)
-                *reinterpret_cast<float4*>(dst + ch * 32 + e) =
-                    make_float4(__uint_as_float(o[ch][e]) * inv, __uint_as_float(o[ch][e + 1]) * inv,
-                                __uint_as_float(o[ch][e + 2]) * inv, __uint_as_float(o[ch][e + 3]) * inv);
-          } else {
-            uint16_t* dst = reinterpret_cast<uint16_t*>(p.out) + (tok * p.hq + head) * DH + half * (DH / 2);
-#pragma unroll
-            for (int ch = 0; ch < CH; ++ch)
-#pragma unroll
-              for (int e = 0; e < 32; e += 8) {
-                uint4 v;
-                v.x = pack_bf16x2(__uint_as_float(o[ch][e]) * inv, __uint_as_float(o[ch][e + 1]) * inv);
-                v.y = pack_bf16x2(__uint_as_float(o[ch][e + 2]) * inv, __uint_as_float(o[ch][e + 3]) * inv);
-                v.z = pack_bf16x2(__uint_as_float(o[ch][e + 4]) * inv, __uint_as_float(o[ch][e + 5]) * inv);
-                v.w = pack_bf16x2(__uint_as_float(o[ch][e + 6]) * inv, __uint_as_float(o[ch][e + 7]) * inv);
-                *reinterpret_cast<uint4*>(dst + ch * 32 + e) = v;
-              }
-          }
-        } else {
-          // kept in L2 for the combine pass, which reads them after the streaming
-          const uint64_t pol_keep = l2_policy_evict_last();
-          float* dst = p.part_o + (static_cast<int64_t>(sg.slot) * kTileRows + rho) * DH + half * (DH / 2);
-#pragma unroll
-          for (int ch = 0; ch < CH; ++ch)
-#pragma unroll
-            for (int e = 0; e < 32; e += 4)
-              st_global_v4_hint(dst + ch * 32 + e,
-                                make_float4(__uint_as_float(o[ch][e]), __uint_as_float(o[ch][e + 1]),
-                                            __uint_as_float(o[ch][e + 2]), __uint_as_float(o[ch][e + 3])),
-                                pol_keep);
-          if (half == 0)
-            st_global_v2_hint(p.part_ml + (static_cast<int64_t>(sg.slot) * kTileRows + rho) * 2, m_used, l_tot, pol_keep);
+       }
+        if (j == 0 && pend.valid()) {  // the previous segment's epilogue, now that this one has started
+          if (!(ok = epilogue(pend))) break;
+          pend.state = 0;
         }
       }
+      if (!ok) break;
+      if (!have) continue;
+      // ---------------------------------------------------------- epilogue (deferred)
+      pend.state = 1 | (row_ok ? 2 : 0) | (sg.complete ? 4 : 0) | (iu << 3);
+      pend.m = m_used;
+      pend.l = l;
+      pend.row = (U.qsl + b) * p.hq + U.kvh * p.g + rho % p.g;
       gj += n;
       gv += n;
+      have = it.next(sg);
     }
     if (!ok) atomicOr(&p.hdr[0], kErrTimeout);
   }

@@ -287,3 +287,19 @@ def test_empty_batch_is_a_no_op():
                               torch.ones(64, dtype=torch.bfloat16, device="cuda"),
                               torch.ones(64, dtype=torch.bfloat16, device="cuda"), max_ctx_len=0, max_block_len=1)
     assert out.shape == (0, 4, 64)
+
+
+@pytest.mark.parametrize("flags", [0, 1, 2])
+def test_more_requests_than_one_schedule_scan(flags):
+    # past 1024 requests every CTA scans the requests in several chunks (an even split of the
+    # tiles, and a second pass to find its segments)
+    rng = np.random.default_rng(29)
+    n = 1100
+    ctx = rng.integers(0, 300, n)
+    ctx[::13] = 0
+    blk = rng.integers(1, 17, n)
+    b = W.make_batch(cfg(8, 2, 64, seed=29), ctx_lens=ctx, block_lens=blk)
+    ck = U.stored_ctx_k(b)
+    want = U.oracle_attention(b, ck)
+    got = U.dev_to_f64(U.gpu_attention(b, ck, flags=flags))
+    U.assert_close_bf16(got, want, f"1100 requests flags={flags}")
