@@ -18,6 +18,11 @@ block key's K and V read once per (request, kv head)), with TFLOP/s and the frac
 of the GB300 roofline beside it. L2 is flushed (256 MB write) before every step,
 outside the timed events.
 
+The timed step runs the largest workload (ragged: 64 requests, contexts log-uniform in
+[1024, 32768]) by default. The same JSON line also carries, each timed the same way with its
+own clock record: "per_workload" (the Qwen3-4B-shaped layer and the sliding-window layer),
+"context_store" (dflash_context_kv building the whole context store) and "draft_step_ops".
+
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
 """
 from __future__ import annotations
@@ -69,7 +74,8 @@ def algorithmic_counts(cfg: W.Config, ctx_lens, block_lens) -> dict:
             "flops": 4 * cfg.dh * pairs * cfg.hq}
 
 
-def describe(cfg: W.Config, ctx_lens) -> dict:
+def describe(cfg: W.Config, ctx_lens, paged: int = 0, world: int = 1) -> dict:
+    """The workload's config dict, the same in both arms."""
     mask = "bidirectional" if not cfg.causal else (f"causal, window {cfg.window}" if cfg.window else "causal")
     if cfg.ctx_len is not None:
         c = str(cfg.ctx_len)
@@ -79,8 +85,13 @@ def describe(cfg: W.Config, ctx_lens) -> dict:
         c = f"log-uniform[{cfg.ctx_loguniform[0]},{cfg.ctx_loguniform[1]}] (sum {int(sum(ctx_lens))})"
     return {"workload": cfg.name + ": " + cfg.note, "requests": cfg.num_reqs, "ctx_len": c, "block": cfg.block,
             "hq": cfg.hq, "hkv": cfg.hkv, "dh": cfg.dh, "mask": mask, "seed": cfg.seed,
+            "split_kv": "forced" if cfg.force_split else "balanced schedule",
             "appended_rows_per_request": cfg.block,
-            "l2": "flushed before every step (256 MB write, outside the timed events)"}
+            "l2": "flushed before every step (256 MB write, outside the timed events)",
+            "context": (f"paged: {paged}-row pages in shuffled order, block table per request; the step's append "
+                        "(dflash_paged_append) advances the device lengths the attention reads, and they are put "
+                        "back between steps outside the timed events" if paged else "contiguous segments"),
+            "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"}
 
 
 def load_peaks() -> tuple[dict, str]:
@@ -138,14 +149,30 @@ class ClockSampler:
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
     def __init__(self, device_index: int):
+        """Starts nvidia-smi (one sample every 20 ms) and waits, up to 3 s, for its first
+        sample, so that the record covers the work launched after this returns."""
+        import threading
         self.proc = None
         self.dev = device_index
+        self.lines: list[str] = []
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(device_index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
                  "-lms", "20"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except Exception:
             self.proc = None
+            return
+        first = threading.Event()
+
+        def reader():
+            for line in self.proc.stdout:
+                self.lines.append(line)
+                first.set()
+            first.set()
+
+        self.thread = threading.Thread(target=reader, daemon=True)
+        self.thread.start()
+        first.wait(timeout=3.0)
 
     def stop(self):
         if self.proc is None:
@@ -153,10 +180,12 @@ class ClockSampler:
         time.sleep(0.03)
         self.proc.terminate()
         try:
-            out, _ = self.proc.communicate(timeout=5)
+            self.proc.wait(timeout=5)
         except Exception:
             self.proc.kill()
             return None
+        self.thread.join(timeout=2)
+        out = "".join(self.lines)
         sm, mx, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for line in out.strip().splitlines():
@@ -300,6 +329,120 @@ class Step:
         return (2 if self.page_size else 1) + int(self.plan["launches"])
 
 
+def timed_steps(st: "Step", flush, stream, steps: int, warmup: int, barrier, dev_index: int,
+                window_s: float) -> tuple[list, list, dict | None]:
+    """Warm-up, then `steps` timed steps (CUDA events around the append and the attention
+    call, L2 flushed before each step outside the events), then a clock window: the same
+    step repeated for about `window_s` seconds, untimed by the result but sampled, so that the
+    nvidia-smi record (20 ms period) spans the timed steps with enough samples. Returns the
+    per-step and per-call times (ms) and the clock record (with the window's mean step time
+    and time x MHz)."""
+    import torch
+    for _ in range(warmup):
+        flush.zero_()
+        st.reset()
+        st.append()
+        st.attend()
+    torch.cuda.synchronize()
+    barrier()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(dev_index)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+    # untimed GPU work queued first, so that the host is ahead of the GPU when the first timed
+    # step starts (otherwise its launch latency shows up between the events)
+    for _ in range(3):
+        flush.zero_()
+    for i in range(steps):
+        flush.zero_()
+        st.reset()
+        ev[i][0].record(stream)
+        st.append()
+        ev[i][1].record(stream)
+        st.attend()
+        ev[i][2].record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    torch.cuda.synchronize()
+    step_ms = [e[0].elapsed_time(e[2]) for e in ev]
+    attn_ms = [e[1].elapsed_time(e[2]) for e in ev]
+    # clock window
+    win_ms, n_win = 0.0, 0
+    if window_s > 0:
+        w0, w1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        n_win = max(1, int(window_s * 1e3 / max(1e-3, statistics.mean(step_ms) + 0.08)))
+        w0.record(stream)
+        for _ in range(n_win):
+            flush.zero_()
+            st.reset()
+            st.append()
+            st.attend()
+        w1.record(stream)
+        torch.cuda.synchronize()
+        win_ms = w0.elapsed_time(w1)
+    clk = clocks.stop()
+    if clk is not None and n_win:
+        per = win_ms / n_win
+        clk["window"] = {"steps": n_win, "ms_per_step_incl_flush": per,
+                         "us_x_mhz_per_step": per * 1e3 * clk["sm_mhz"]}
+    return step_ms, attn_ms, clk
+
+
+def attention_entry(cfg: W.Config, b: W.Batch, attn_ms: list, peaks: dict, peak_note: str, paged: int,
+                    clk) -> dict:
+    counts = algorithmic_counts(cfg, b.ctx_lens, b.block_lens)
+    avg_s = statistics.mean(attn_ms) / 1e3
+    achieved = counts["kv_bytes"] / avg_s / 1e9
+    return {
+        "bound": "hbm",
+        "kernel": "dflash_block_attention call (prologue + attention + combine launches)",
+        "achieved": achieved,
+        "peak": peaks["hbm_gbs"],
+        "unit": "GB/s",
+        "frac": achieved / peaks["hbm_gbs"],
+        "peak_source": peak_note,
+        "traffic": recorded_traffic(cfg.name + (f"_paged{paged}" if paged else "")),
+        "algorithmic_bytes_per_launch": counts["kv_bytes"],
+        "call_us": avg_s * 1e6,
+        "tensor_tflops": counts["flops"] / avg_s / 1e12,
+        "tensor_frac": counts["flops"] / avg_s / 1e12 / peaks["bf16_tflops"],
+        **({"clocks": clk} if clk is not None else {}),
+    }
+
+
+def time_context_store(lib, b: W.Batch, st: "Step", flush, stream, steps: int, peaks: dict, peak_note: str) -> dict:
+    """dflash_context_kv over the whole context (every row of the store: K normed + rotated,
+    V copied), timed on its own: algorithmic bytes = K and V read and written, 4 * rows * Hkv *
+    Dh * 2 B."""
+    import numpy as np
+    import torch
+    c = b.cfg
+    k_raw = st.d16(b.ctx_k_raw)
+    v_raw = st.d16(b.ctx_v)
+    pos = st.d32(b.ctx_pos)
+    n = b.ctx_k_raw.shape[0]
+    ck = torch.empty((n, c.hkv, c.dh), dtype=torch.bfloat16, device="cuda")
+    cv = torch.empty_like(ck)
+    call = lambda: lib.context_kv(k_raw, pos, st.k_norm_w, ck, v=v_raw, ctx_v=cv, eps=c.eps, theta=c.theta)  # noqa: E731
+    for _ in range(3):
+        flush.zero_()
+        call()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(steps)]
+    for i in range(steps):
+        flush.zero_()
+        ev[i][0].record(stream)
+        call()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    us = statistics.mean(e[0].elapsed_time(e[1]) for e in ev) * 1e3
+    nbytes = 4 * n * c.hkv * c.dh * 2
+    achieved = nbytes / (us * 1e-6) / 1e9
+    del k_raw, v_raw, ck, cv
+    return {"kernel": "dflash_context_kv (norm_rope_kernel), the whole context store", "rows": int(n),
+            "us": us, "bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+            "frac": achieved / peaks["hbm_gbs"], "peak_source": peak_note,
+            "algorithmic_bytes_per_launch": nbytes}
+
+
 def run_gpu(args, b: W.Batch, rank: int, world: int) -> dict | None:
     import numpy as np
     import torch
@@ -314,42 +457,16 @@ def run_gpu(args, b: W.Batch, rank: int, world: int) -> dict | None:
     counts = algorithmic_counts(cfg, b.ctx_lens, b.block_lens)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
     stream = torch.cuda.current_stream()
+    peaks, peak_note = load_peaks()
 
     def barrier():
         if world > 1:
             import torch.distributed as dist
             dist.barrier()
 
-    # ---- warm-up
-    for _ in range(args.warmup):
-        flush.zero_()
-        st.reset()
-        st.append()
-        st.attend()
-    torch.cuda.synchronize()
-    barrier()
-    torch.cuda.synchronize()
-    clocks = ClockSampler(dev_index)
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
-    # untimed GPU work queued first, so that the host is ahead of the GPU when the first timed
-    # step starts (otherwise its launch latency shows up between the events)
-    for _ in range(3):
-        flush.zero_()
-    for i in range(args.steps):
-        flush.zero_()
-        st.reset()
-        ev[i][0].record(stream)
-        st.append()
-        ev[i][1].record(stream)
-        st.attend()
-        ev[i][2].record(stream)
-    torch.cuda.synchronize()
-    barrier()
-    torch.cuda.synchronize()
-    clk = clocks.stop()
+    step_ms, attn_ms, clk = timed_steps(st, flush, stream, args.steps, args.warmup, barrier, dev_index,
+                                        args.clock_window)
     lib.check_error(st.ws)
-    step_ms = [e[0].elapsed_time(e[2]) for e in ev]
-    attn_ms = [e[1].elapsed_time(e[2]) for e in ev]
     total_ms = sum(step_ms)
     total_ms = max_over_ranks(total_ms, device="cuda")
 
@@ -387,10 +504,8 @@ def run_gpu(args, b: W.Batch, rank: int, world: int) -> dict | None:
     st.seq_lens = device_lens
 
     ops = time_draft_ops(lib, b, flush, stream, args.steps)
-
-    peaks, peak_note = load_peaks()
-    attn_avg_s = statistics.mean(attn_ms) / 1e3
-    achieved = counts["kv_bytes"] / attn_avg_s / 1e9
+    store = time_context_store(lib, b, st, flush, stream, args.steps, peaks, peak_note)
+    roof = attention_entry(cfg, b, attn_ms, peaks, peak_note, args.paged, None)
     res = {
         "metric": METRIC,
         "value": world * counts["kv_bytes"] * args.steps / (total_ms / 1e3) / 1e9,
@@ -404,36 +519,39 @@ def run_gpu(args, b: W.Batch, rank: int, world: int) -> dict | None:
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic",
-        "config": {**describe(cfg, b.ctx_lens),
-                   "context": (f"paged: {args.paged}-row pages in shuffled order, block table per request; the "
-                               "step's append (dflash_paged_append) advances the device lengths the attention "
-                               "reads, and they are put back between steps outside the timed events"
-                               if args.paged else "contiguous segments"),
-                   "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"},
+        "config": describe(cfg, b.ctx_lens, args.paged, world),
         "tflops": world * counts["flops"] * args.steps / (total_ms / 1e3) / 1e12,
         "attention_ms": statistics.mean(attn_ms),
         "append_ms": statistics.mean(s - a for s, a in zip(step_ms, attn_ms)),
-        "roofline": {
-            "bound": "hbm",
-            "kernel": "dflash_block_attention call (prologue + attention + combine launches)",
-            "achieved": achieved,
-            "peak": peaks["hbm_gbs"],
-            "unit": "GB/s",
-            "frac": achieved / peaks["hbm_gbs"],
-            "peak_source": peak_note,
-            "traffic": recorded_traffic(cfg.name + (f"_paged{args.paged}" if args.paged else "")),
-            "algorithmic_bytes_per_launch": counts["kv_bytes"],
-            "tensor_tflops": counts["flops"] / attn_avg_s / 1e12,
-            "tensor_frac": counts["flops"] / attn_avg_s / 1e12 / peaks["bf16_tflops"],
-        },
+        "roofline": roof,
         "e2e": {"value": world * counts["kv_bytes"] * args.steps / (e2e_ms / 1e3) / 1e9, "unit": "GB/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "host_inputs": "one pinned staging buffer, one host-to-device copy per step"},
         "gpu_launches": st.launches_per_step() * args.steps,
         "clocks": clk,
         "plan": st.plan,
+        "context_store": store,
         "draft_step_ops": ops,
     }
+    del st, staging
+    torch.cuda.empty_cache()
+    # ---- the other long-context workloads of the target (Qwen3-4B-shaped and SWA layers),
+    # each timed the same way with its own clock record
+    if not args.paged and not args.no_per_workload:
+        per = {}
+        for name in ("qwen3_4b", "swa", "ragged"):
+            if name == cfg.name:
+                continue
+            bw = W.make_batch(W.CONFIGS[name])
+            sw = Step(lib, bw, lib.FLAG_FORCE_SPLIT if bw.cfg.force_split else 0, 0)
+            _, am, ck = timed_steps(sw, flush, stream, args.steps, args.warmup, barrier, dev_index,
+                                    args.clock_window)
+            lib.check_error(sw.ws)
+            per[name] = {"config": describe(bw.cfg, bw.ctx_lens, 0, world),
+                         "roofline": attention_entry(bw.cfg, bw, am, peaks, peak_note, 0, ck)}
+            del sw
+            torch.cuda.empty_cache()
+        res["per_workload"] = per
     return res
 
 
@@ -587,7 +705,7 @@ def run_reference(args, b: W.Batch) -> dict:
         "vs_baseline": None,
         "dtype": "f64",
         "data": "synthetic",
-        "config": describe(cfg, b.ctx_lens),
+        "config": describe(cfg, b.ctx_lens, args.paged, int(os.environ.get("WORLD_SIZE", "1"))),
         "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": desc},
         "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -598,9 +716,14 @@ def main() -> int:
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--workload", default="qwen3_4b", choices=sorted(W.CONFIGS))
+    ap.add_argument("--workload", default="ragged", choices=sorted(W.CONFIGS),
+                    help="the timed step's workload (default: the largest, the ragged long-context batch)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-workload", action="store_true",
+                    help="skip timing the other long-context workloads beside the main one")
+    ap.add_argument("--clock-window", type=float, default=0.3,
+                    help="seconds of repeated steps after the timed ones, sampled for the clock record")
     ap.add_argument("--paged", type=int, default=0, choices=[0, 16, 32, 64, 128],
                     help="context in a page pool of this many rows per page (shuffled page order); 0: contiguous")
     args = ap.parse_args()

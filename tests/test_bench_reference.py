@@ -30,6 +30,9 @@ def test_reference_line_follows_the_contract():
     assert d["cpu_baseline"]["value"] == d["value"]
     assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
     assert d["config"]["workload"].startswith("tiny")
+    # the same config keys as the GPU arm's line
+    assert set(d["config"]) == {"workload", "requests", "ctx_len", "block", "hq", "hkv", "dh", "mask", "seed",
+                                "split_kv", "appended_rows_per_request", "l2", "context", "parallelism"}
 
 
 def test_reference_arm_prints_only_on_rank_0():
