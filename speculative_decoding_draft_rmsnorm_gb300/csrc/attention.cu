@@ -597,6 +597,11 @@ __device__ __forceinline__ void produce_paged(const AttnParams& p, const CUtenso
   }
 }
 
+#ifdef DFLASH_WAIT_TEST
+// Test build only: (CTA, V tile count) of one V tile whose copy the producer withholds.
+__device__ int2 g_withhold_v = {-1, -1};
+#endif
+
 template <int DH, int NK, int NV, int NQ, bool PRECISE, bool PAGED>
 __global__ void __launch_bounds__(192, 1)
 attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_kc,
@@ -738,6 +743,12 @@ attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         auto issue_v = [&](int t) -> bool {
           const int slot = static_cast<int>(gv % NV);
           if (!mbar_wait(bar(L::V_EMPTY + slot), ((gv / NV) & 1) ^ 1, abort_flag)) return false;
+#ifdef DFLASH_WAIT_TEST
+          if (static_cast<int>(blockIdx.x) == g_withhold_v.x && static_cast<int>(gv) == g_withhold_v.y) {
+            ++gv;  // this tile's copy is never issued: its consumer's wait must run out
+            return true;
+          }
+#endif
           const TileInfo ti = tile_info(U, t, p.blk_tile);
           mbar_arrive_expect_tx(bar(L::V_FULL + slot), L::KB);
           const void* map = ti.blk ? static_cast<const void*>(&tm_vb) : static_cast<const void*>(&tm_vc);
@@ -1491,3 +1502,13 @@ cudaError_t launch_attention(const AttnHost& h, cudaStream_t stream, char* msg, 
 }
 
 }  // namespace dflash
+
+#ifdef DFLASH_WAIT_TEST
+// Test build only: makes the producer of CTA `cta` skip the copy of its `tile`-th V tile
+// (counted from 0 over the CTA's whole pass) in the following attention calls; cta = -1
+// turns it off. Returns a cudaError_t.
+extern "C" __attribute__((visibility("default"))) int dflash_test_withhold_v_tile(int cta, int tile) {
+  const int2 v = make_int2(cta, tile);
+  return static_cast<int>(cudaMemcpyToSymbol(dflash::g_withhold_v, &v, sizeof v));
+}
+#endif

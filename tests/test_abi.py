@@ -34,6 +34,18 @@ def test_library_loads_and_exports_every_declared_symbol():
     for n in declared_symbols():
         assert hasattr(raw, n), f"{n} is declared in include/ but not exported"
     assert lib.dflash_version() >> 16 == 1
+    # the test build's hook (a withheld copy, see test_gpu_wait_timeout.py) is not in the product
+    assert not hasattr(raw, "dflash_test_withhold_v_tile")
+
+
+def test_wait_test_library_is_the_product_plus_the_hook():
+    from speculative_decoding_draft_rmsnorm_gb300 import _build
+    if not _build.up_to_date(_build.WAIT_TEST_LIB_PATH):
+        _build.build()
+    raw = ctypes.CDLL(_build.WAIT_TEST_LIB_PATH)
+    assert hasattr(raw, "dflash_test_withhold_v_tile")
+    for n in declared_symbols():
+        assert hasattr(raw, n), n
 
 
 def _attn(**over):
