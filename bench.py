@@ -329,6 +329,13 @@ class Step:
         return (2 if self.page_size else 1) + int(self.plan["launches"])
 
 
+def gpu_spin(seconds: float) -> None:
+    """Queues a kernel that keeps the GPU busy for about `seconds` (SM clock cycles at the
+    maximum clock), so that the host can queue the following launches ahead of the GPU."""
+    import torch
+    torch.cuda._sleep(int(seconds * 2.07e9))
+
+
 def timed_steps(st: "Step", flush, stream, steps: int, warmup: int, barrier, dev_index: int,
                 window_s: float) -> tuple[list, list, dict | None]:
     """Warm-up, then `steps` timed steps (CUDA events around the append and the attention
@@ -348,10 +355,11 @@ def timed_steps(st: "Step", flush, stream, steps: int, warmup: int, barrier, dev
     torch.cuda.synchronize()
     clocks = ClockSampler(dev_index)
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
-    # untimed GPU work queued first, so that the host is ahead of the GPU when the first timed
-    # step starts (otherwise its launch latency shows up between the events)
-    for _ in range(3):
-        flush.zero_()
+    # untimed GPU work queued first (a spin of about 0.3 ms per step to come), so that the host
+    # has queued every timed step before the GPU reaches the first one: the host's own time per
+    # step (Python argument checks, tensor-map encoding, launches) then never shows up as GPU
+    # idle time between the events
+    gpu_spin(0.3e-3 * steps)
     for i in range(steps):
         flush.zero_()
         st.reset()
@@ -427,6 +435,7 @@ def time_context_store(lib, b: W.Batch, st: "Step", flush, stream, steps: int, p
         flush.zero_()
         call()
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(steps)]
+    gpu_spin(0.2e-3 * steps)
     for i in range(steps):
         flush.zero_()
         ev[i][0].record(stream)
@@ -577,6 +586,7 @@ def time_draft_ops(lib, b: W.Batch, flush, stream, steps: int) -> dict:
             if reset:
                 reset()
             fn()
+        gpu_spin(0.2e-3 * steps)
         for i in range(steps):
             flush.zero_()
             if reset:

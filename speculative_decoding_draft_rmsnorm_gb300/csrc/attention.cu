@@ -358,6 +358,15 @@ __global__ void __launch_bounds__(256, 3) prologue_kernel(const __grid_constant_
 }
 
 // ================================================================ kernel B
+// A partial slot (64 rows x DH f32) is stored in the order the softmax threads hold it: the
+// thread of TMEM sub-partition sp and lane L (row 16 sp + L % 16, columns from (L / 16) DH / 2)
+// writes its k-th 4-float group (columns + 4k .. 4k + 3) at float4 index
+// (sp DH / 8 + k) 32 + L, so that each warp store covers 512 contiguous bytes.
+template <int DH>
+__device__ __forceinline__ int64_t part_o_index(int sp, int k, int lane) {
+  return (static_cast<int64_t>(sp) * (DH / 8) + k) * 32 + lane;
+}
+
 // Shared-memory plan. NQ query buffers (hi, and lo in precise mode), two P buffers (hi,
 // and lo in precise mode), an NK-stage K ring and an NV-stage V ring; 1024-byte aligned
 // tiles (128-byte swizzle atoms).
@@ -959,12 +968,14 @@ attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         // kept in L2 for the combine pass, which reads them after the streaming
         const uint64_t pol_keep = l2_policy_evict_last();
         const int pslot = 2 * static_cast<int>(blockIdx.x) + (e_iu == 0 ? 0 : 1);  // first segment, or later
-        float* dst = p.part_o + (static_cast<int64_t>(pslot) * kTileRows + rho) * DH + half * (DH / 2);
+        // the slot is laid out in the order the threads hold it (part_o_index): every store
+        // instruction of the warp writes 512 contiguous bytes
+        float* dst = p.part_o + (static_cast<int64_t>(pslot) * kTileRows * DH) + part_o_index<DH>(sp, 0, lane) * 4;
 #pragma unroll
         for (int ch = 0; ch < CH; ++ch)
 #pragma unroll
           for (int x = 0; x < 32; x += 4)
-            st_global_v4_hint(dst + ch * 32 + x,
+            st_global_v4_hint(dst + (ch * 8 + x / 4) * 32 * 4,
                               make_float4(__uint_as_float(o[ch][x]), __uint_as_float(o[ch][x + 1]),
                                           __uint_as_float(o[ch][x + 2]), __uint_as_float(o[ch][x + 3])),
                               pol_keep);
@@ -1181,65 +1192,67 @@ __global__ void __launch_bounds__(256) combine_kernel(const __grid_constant__ At
   if (!mine) return;
   // the group is CTA b's first segment iff it starts at lo0
   const bool ca_first = G.start == lo0;
-  constexpr int CPR = DH / 8;   // 8-float chunks per row; block y covers rows [16y, 16y+16)
+  // Block y covers rows [16y, 16y + 16): thread t merges the 4-float groups k0 = t / 32 and
+  // k0 + DH / 16 that lane t % 32 of TMEM sub-partition y stored (part_o_index), so that every
+  // load of a warp reads 512 contiguous bytes.
   constexpr int kMaxBatch = 2;  // contributors whose loads are in flight together
-  for (int item = threadIdx.x; item < 16 * CPR; item += blockDim.x) {
-    const int rho = 16 * static_cast<int>(blockIdx.y) + item / CPR;
-    if (rho >= G.rows) break;
-    const int c8 = (item % CPR) * 8;
-    // running merge: o = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s, contributors in batches
-    float M = -INFINITY, L = 0.0f;
-    float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-    for (long long c = ca; c <= cb; c += kMaxBatch) {
-      float2 ml[kMaxBatch];
-      float4 oa[kMaxBatch], ob[kMaxBatch];
+  const int lane = static_cast<int>(threadIdx.x & 31);
+  const int rho = 16 * static_cast<int>(blockIdx.y) + (lane & 15);
+  if (rho >= G.rows) return;
+  const int k0 = static_cast<int>(threadIdx.x >> 5);
+  // running merge: o = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s, contributors in batches
+  float M = -INFINITY, L = 0.0f;
+  float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+  for (long long c = ca; c <= cb; c += kMaxBatch) {
+    float2 ml[kMaxBatch];
+    float4 oa[kMaxBatch], ob[kMaxBatch];
 #pragma unroll
-      for (int i = 0; i < kMaxBatch; ++i) {
-        const long long cc = c + i;
-        if (cc <= cb) {
-          const long long slot = 2 * cc + ((cc == ca && !ca_first) ? 1 : 0);
-          ml[i] = __ldcg(reinterpret_cast<const float2*>(p.part_ml + (slot * kTileRows + rho) * 2));
-          const float4* src = reinterpret_cast<const float4*>(p.part_o + (slot * kTileRows + rho) * DH + c8);
-          oa[i] = __ldcg(src);
-          ob[i] = __ldcg(src + 1);
-        } else {
-          ml[i] = make_float2(-INFINITY, 0.0f);
-          oa[i] = ob[i] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-        }
+    for (int i = 0; i < kMaxBatch; ++i) {
+      const long long cc = c + i;
+      if (cc <= cb) {
+        const long long slot = 2 * cc + ((cc == ca && !ca_first) ? 1 : 0);
+        ml[i] = __ldcg(reinterpret_cast<const float2*>(p.part_ml + (slot * kTileRows + rho) * 2));
+        const float4* src =
+            reinterpret_cast<const float4*>(p.part_o + slot * kTileRows * DH) + part_o_index<DH>(blockIdx.y, k0, lane);
+        oa[i] = __ldcg(src);
+        ob[i] = __ldcg(src + (DH / 16) * 32);
+      } else {
+        ml[i] = make_float2(-INFINITY, 0.0f);
+        oa[i] = ob[i] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
       }
-      float Mn = M;
-#pragma unroll
-      for (int i = 0; i < kMaxBatch; ++i) Mn = fmaxf(Mn, ml[i].x);
-      if (Mn == -INFINITY) continue;
-      const float r = M == -INFINITY ? 0.0f : ex2_approx(M - Mn);
-      L *= r;
-#pragma unroll
-      for (int e = 0; e < 8; ++e) acc[e] *= r;
-#pragma unroll
-      for (int i = 0; i < kMaxBatch; ++i) {
-        const float w = ml[i].x == -INFINITY ? 0.0f : ex2_approx(ml[i].x - Mn);
-        L += w * ml[i].y;
-        acc[0] += w * oa[i].x; acc[1] += w * oa[i].y; acc[2] += w * oa[i].z; acc[3] += w * oa[i].w;
-        acc[4] += w * ob[i].x; acc[5] += w * ob[i].y; acc[6] += w * ob[i].z; acc[7] += w * ob[i].w;
-      }
-      M = Mn;
     }
-    const float inv = L > 0.0f ? 1.0f / L : 0.0f;
-    const int64_t tok = G.qsl + G.tok0 + rho / p.g;
-    const int head = G.kvh * p.g + rho % p.g;
-    if (p.out_f32) {
-      float* dst = reinterpret_cast<float*>(p.out) + (tok * p.hq + head) * DH + c8;
-      *reinterpret_cast<float4*>(dst) = make_float4(acc[0] * inv, acc[1] * inv, acc[2] * inv, acc[3] * inv);
-      *reinterpret_cast<float4*>(dst + 4) = make_float4(acc[4] * inv, acc[5] * inv, acc[6] * inv, acc[7] * inv);
-    } else {
-      uint16_t* dst = reinterpret_cast<uint16_t*>(p.out) + (tok * p.hq + head) * DH + c8;
-      uint4 v;
-      v.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
-      v.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
-      v.z = pack_bf16x2(acc[4] * inv, acc[5] * inv);
-      v.w = pack_bf16x2(acc[6] * inv, acc[7] * inv);
-      *reinterpret_cast<uint4*>(dst) = v;
+    float Mn = M;
+#pragma unroll
+    for (int i = 0; i < kMaxBatch; ++i) Mn = fmaxf(Mn, ml[i].x);
+    if (Mn == -INFINITY) continue;
+    const float r = M == -INFINITY ? 0.0f : ex2_approx(M - Mn);
+    L *= r;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) acc[e] *= r;
+#pragma unroll
+    for (int i = 0; i < kMaxBatch; ++i) {
+      const float w = ml[i].x == -INFINITY ? 0.0f : ex2_approx(ml[i].x - Mn);
+      L += w * ml[i].y;
+      acc[0] += w * oa[i].x; acc[1] += w * oa[i].y; acc[2] += w * oa[i].z; acc[3] += w * oa[i].w;
+      acc[4] += w * ob[i].x; acc[5] += w * ob[i].y; acc[6] += w * ob[i].z; acc[7] += w * ob[i].w;
     }
+    M = Mn;
+  }
+  const float inv = L > 0.0f ? 1.0f / L : 0.0f;
+  const int64_t tok = G.qsl + G.tok0 + rho / p.g;
+  const int head = G.kvh * p.g + rho % p.g;
+  const int64_t col_a = (lane >> 4) * (DH / 2) + 4 * k0;  // columns of the first group
+  const int64_t col_b = col_a + 4 * (DH / 16);             // and of the second
+  if (p.out_f32) {
+    float* row = reinterpret_cast<float*>(p.out) + (tok * p.hq + head) * DH;
+    *reinterpret_cast<float4*>(row + col_a) = make_float4(acc[0] * inv, acc[1] * inv, acc[2] * inv, acc[3] * inv);
+    *reinterpret_cast<float4*>(row + col_b) = make_float4(acc[4] * inv, acc[5] * inv, acc[6] * inv, acc[7] * inv);
+  } else {
+    uint16_t* row = reinterpret_cast<uint16_t*>(p.out) + (tok * p.hq + head) * DH;
+    *reinterpret_cast<uint2*>(row + col_a) = make_uint2(pack_bf16x2(acc[0] * inv, acc[1] * inv),
+                                                        pack_bf16x2(acc[2] * inv, acc[3] * inv));
+    *reinterpret_cast<uint2*>(row + col_b) = make_uint2(pack_bf16x2(acc[4] * inv, acc[5] * inv),
+                                                        pack_bf16x2(acc[6] * inv, acc[7] * inv));
   }
 }
 

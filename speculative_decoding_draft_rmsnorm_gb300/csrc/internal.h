@@ -115,7 +115,7 @@ struct AttnHost {
   uint16_t *q_hat, *q_lo, *k_hat, *k_lo;
   Group* groups;
   CtaRecord* cta_rec; // [grid] balanced schedule only
-  float* part_o;      // [2 * grid][64][dh]  partial O of straddling segments
+  float* part_o;      // [2 * grid][64 * dh]  partial O of straddling segments (in thread order)
   float* part_ml;     // [2 * grid][64][2]   their running max (log2 units) and weight sum
   RopeTurns turns;
 };
