@@ -367,6 +367,16 @@ __device__ __forceinline__ int64_t part_o_index(int sp, int k, int lane) {
   return (static_cast<int64_t>(sp) * (DH / 8) + k) * 32 + lane;
 }
 
+// A K or V tile normally sits in shared memory as DH / 64 column blocks of 128 rows x 128
+// bytes (128-byte swizzle), one TMA box per column block (and page). With 16-row pages and
+// Dh = 128 that is 32 boxes of 2 KB per K + V tile, and the per-box cost of the TMA unit, not
+// HBM, sets the rate. Paged context tiles with Dh = 128 are instead stored group-major: rows
+// 8i .. 8i + 7 at i * kGroupBytes, column block nb at + nb * 1 KB, so that one box brings a
+// whole page (16 boxes a tile, whatever the page size). The 8-row groups are still evenly
+// spaced, now kGroupBytes apart, which is all the MMA descriptors need: S = Q K^T still takes
+// the 128 keys in one MMA per 16 columns and PV 16 keys per MMA.
+constexpr uint32_t kGroupBytes = 2048;  // one 8-row group of both 64-column blocks
+
 // Shared-memory plan. NQ query buffers (hi, and lo in precise mode), two P buffers (hi,
 // and lo in precise mode), an NK-stage K ring and an NV-stage V ring; 1024-byte aligned
 // tiles (128-byte swizzle atoms).
@@ -408,6 +418,7 @@ struct AttnParams {
   float* part_ml;
   void* out;
   int hq, g, out_f32, causal, window, blk_tile;
+  int grp_major;  // paged context K / V tiles laid out 8-row group by group in shared memory
   int balanced;  // stream-K schedule (else one whole group per CTA, round-robin)
   int grid;      // CTAs of the attention kernel (the combine kernel recomputes their ranges)
   float scale_log2;
@@ -566,13 +577,20 @@ __device__ __forceinline__ void produce_paged(const AttnParams& p, const CUtenso
           atomicOr(&p.hdr[0], kErrMetadata);
           pg = 0;
         }
-        // one box per lane: lane b copies 64-column half b % NB of page b / NB
-        const int my_page = __shfl_sync(0xffffffffu, pg, (lane / L::NB) & 31);
-        if (lane < nsub * L::NB) {
-          const int sp = lane / L::NB, nb = lane % L::NB;
-          const void* map = is_k ? static_cast<const void*>(tm_kc) : static_cast<const void*>(tm_vc);
-          tma_load_3d_hint(dst + nb * (kTileKeys * 128) + sp * ps * 128, map, full, nb * 64, U.kvh, my_page * ps,
-                           pol_stream);
+        const void* map = is_k ? static_cast<const void*>(tm_kc) : static_cast<const void*>(tm_vc);
+        if (p.grp_major) {
+          // one box per lane: lane b copies page b whole, ps / 8 row groups
+          if (lane < nsub)
+            tma_load_5d_hint(dst + lane * (ps / 8) * kGroupBytes, map, full, 0, 0, 0, pg * (ps / 8), U.kvh,
+                             pol_stream);
+        } else {
+          // one box per lane: lane b copies 64-column half b % NB of page b / NB
+          const int my_page = __shfl_sync(0xffffffffu, pg, (lane / L::NB) & 31);
+          if (lane < nsub * L::NB) {
+            const int sp = lane / L::NB, nb = lane % L::NB;
+            tma_load_3d_hint(dst + nb * (kTileKeys * 128) + sp * ps * 128, map, full, nb * 64, U.kvh, my_page * ps,
+                             pol_stream);
+          }
         }
       }
       if (is_k) ++gk; else ++gv;
@@ -826,11 +844,15 @@ attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         const int nq = min(kTileKeys, (ti.valid + 15) & ~15);
         const uint32_t idesc = umma_idesc_bf16(kTileRows, nq, 0, 0);
         const uint32_t k_addr = sbase + L::OFF_K + slot * L::KB;
+        // group-major paged context tiles: column block nb at nb * 1 KB, 8-row groups 2 KB apart
+        const bool gm = PAGED && p.grp_major && !ti.blk;
+        const uint32_t k_nb = gm ? 1024 : kTileKeys * 128;
+        const uint32_t k_sbo = gm ? kGroupBytes : 1024;
 #pragma unroll
         for (int kk = 0; kk < DH / 16; ++kk) {
           const uint32_t qo = (kk >> 2) * (kTileRows * 128) + (kk & 3) * 32;
-          const uint32_t ko = (kk >> 2) * (kTileKeys * 128) + (kk & 3) * 32;
-          const uint64_t b = umma_desc_sw128(k_addr + ko, 16, 1024);
+          const uint32_t ko = (kk >> 2) * k_nb + (kk & 3) * 32;
+          const uint64_t b = umma_desc_sw128(k_addr + ko, 16, k_sbo);
           umma_bf16_ss(tmem + sb * 128, umma_desc_sw128(q_addr + qo, 16, 1024), b, idesc, kk > 0 ? 1u : 0u);
           if (PRECISE) {
             // S = Q_hi K + Q_lo K (+ Q_hi K_lo on block tiles, whose keys are rounded here)
@@ -873,9 +895,14 @@ attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
           const int ksteps = (ti.valid + 15) >> 4;
           const uint32_t p_addr = sbase + L::OFF_P + pb * L::PBT;
           const uint32_t v_addr = sbase + L::OFF_V + vslot * L::KB;
+          // group-major paged context tiles: 16 keys = two groups, column blocks 1 KB apart
+          const bool gm = PAGED && p.grp_major && !ti.blk;
+          const uint32_t v_step = gm ? 2 * kGroupBytes : 16 * 128;
+          const uint32_t v_lbo = gm ? 1024 : kTileKeys * 128;
+          const uint32_t v_sbo = gm ? kGroupBytes : 1024;
           for (int kk = 0; kk < ksteps; ++kk) {
             const uint32_t po = (kk >> 2) * (kTileRows * 128) + (kk & 3) * 32;
-            const uint64_t b = umma_desc_sw128(v_addr + kk * (16 * 128), kTileKeys * 128, 1024);
+            const uint64_t b = umma_desc_sw128(v_addr + kk * v_step, v_lbo, v_sbo);
             umma_bf16_ss(tmem + o_col, umma_desc_sw128(p_addr + po, 16, 1024), b, idesc_pv,
                          (j > 0 || kk > 0) ? 1u : 0u);
             if (PRECISE) umma_bf16_ss(tmem + o_col, umma_desc_sw128(p_addr + L::PB + po, 16, 1024), b, idesc_pv, 1u);
@@ -1121,8 +1148,10 @@ attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             const int row = r0 + c / (L::NB * 8);
             const int rem = c % (L::NB * 8);
             const int nb = rem / 8, chn = rem % 8;
-            *reinterpret_cast<uint4*>(smem + L::OFF_V + vslot * L::KB + nb * (kTileKeys * 128) + row * 128 + chn * 16) =
-                make_uint4(0, 0, 0, 0);
+            const int off = (PAGED && p.grp_major && !ti.blk)
+                                ? (row / 8) * static_cast<int>(kGroupBytes) + nb * 1024 + (row % 8) * 128
+                                : nb * (kTileKeys * 128) + row * 128;
+            *reinterpret_cast<uint4*>(smem + L::OFF_V + vslot * L::KB + off + chn * 16) = make_uint4(0, 0, 0, 0);
           }
         }
         fence_proxy_async_smem();
@@ -1290,6 +1319,24 @@ static bool encode_rows_map(CUtensorMap* m, const void* base, int dh, int heads,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Group-major view of a paged pool [rows, heads, dh] with dh = 128: dimensions {64 columns,
+// 8 rows, 2 column blocks, rows / 8 groups, heads} (strides: row 2 KB-ish, column block 128 B,
+// group 8 rows, head dh * 2), box {64, 8, 2, page_size / 8, 1}: one box lands as the page's
+// 8-row groups, each as its two column blocks one after the other.
+static bool encode_group_major_map(CUtensorMap* m, const void* base, int dh, int heads, int64_t rows, int page_size) {
+  EncodeTiledFn enc = get_encode_fn();
+  if (!enc) return false;
+  const cuuint64_t row_bytes = static_cast<cuuint64_t>(dh) * heads * 2;
+  cuuint64_t dims[5] = {64, 8, static_cast<cuuint64_t>(dh / 64), static_cast<cuuint64_t>(rows > 0 ? rows / 8 : 1),
+                        static_cast<cuuint64_t>(heads)};
+  cuuint64_t strides[4] = {row_bytes, 128, 8 * row_bytes, static_cast<cuuint64_t>(dh) * 2};
+  cuuint32_t box[5] = {64, 8, static_cast<cuuint32_t>(dh / 64), static_cast<cuuint32_t>(page_size / 8), 1};
+  cuuint32_t es[5] = {1, 1, 1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(base), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // rank-4 view {dh, g, hkv, tokens} of q^ [tokens, hkv*g, dh], box {64, g, 1, tpq}
 static bool encode_q_map(CUtensorMap* m, const void* base, int dh, int g, int hkv, int64_t tokens, int tpq) {
   EncodeTiledFn enc = get_encode_fn();
@@ -1447,9 +1494,12 @@ cudaError_t launch_attention(const AttnHost& h, cudaStream_t stream, char* msg, 
   const void* ctx_k = h.total_ctx > 0 ? static_cast<const void*>(h.ctx_k) : static_cast<const void*>(h.q_hat);
   const void* ctx_v = h.total_ctx > 0 ? static_cast<const void*>(h.ctx_v) : static_cast<const void*>(h.q_hat);
   const int64_t ctx_rows = h.total_ctx > 0 ? h.total_ctx : 1;
+  const bool grp_major = h.paged && h.dh == 128;
   bool ok = encode_q_map(&tq, h.q_hat, h.dh, h.g, h.hkv, h.total_q, h.tpq) &&
-            encode_rows_map(&tkc, ctx_k, h.dh, h.hkv, ctx_rows, h.paged ? h.page_size : kTileKeys) &&
-            encode_rows_map(&tvc, ctx_v, h.dh, h.hkv, ctx_rows, h.paged ? h.page_size : kTileKeys) &&
+            (grp_major ? encode_group_major_map(&tkc, ctx_k, h.dh, h.hkv, ctx_rows, h.page_size) &&
+                             encode_group_major_map(&tvc, ctx_v, h.dh, h.hkv, ctx_rows, h.page_size)
+                       : encode_rows_map(&tkc, ctx_k, h.dh, h.hkv, ctx_rows, h.paged ? h.page_size : kTileKeys) &&
+                             encode_rows_map(&tvc, ctx_v, h.dh, h.hkv, ctx_rows, h.paged ? h.page_size : kTileKeys)) &&
             encode_rows_map(&tkb, h.k_hat, h.dh, h.hkv, h.total_q, h.precise ? 64 : kTileKeys) &&
             encode_rows_map(&tvb, h.v_blk, h.dh, h.hkv, h.total_q, kTileKeys);
   if (ok && h.precise)
@@ -1480,6 +1530,7 @@ cudaError_t launch_attention(const AttnHost& h, cudaStream_t stream, char* msg, 
   ap.block_table = h.paged ? h.block_table : nullptr;
   ap.max_pages = h.max_pages;
   ap.page_size = h.paged ? h.page_size : kTileKeys;
+  ap.grp_major = grp_major ? 1 : 0;
   ap.num_pages = h.paged ? h.total_ctx / h.page_size : 0;
   ap.balanced = h.balanced ? 1 : 0;
   ap.grid = h.grid;

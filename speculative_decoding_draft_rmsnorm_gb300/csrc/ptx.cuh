@@ -137,6 +137,15 @@ __device__ __forceinline__ void tma_load_3d_hint(uint32_t dst, const void* tmap,
       : "memory");
 }
 
+__device__ __forceinline__ void tma_load_5d_hint(uint32_t dst, const void* tmap, uint32_t bar, int x, int y, int z,
+                                                 int w, int v, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.5d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7], %8;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(z), "r"(w), "r"(v), "r"(bar), "l"(policy)
+      : "memory");
+}
+
 __device__ __forceinline__ void st_global_v4_hint(float* ptr, float4 v, uint64_t policy) {
   asm volatile("st.global.L2::cache_hint.v4.f32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(ptr), "f"(v.x), "f"(v.y), "f"(v.z),
                "f"(v.w), "l"(policy)
