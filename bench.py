@@ -479,6 +479,32 @@ def run_gpu(args, b: W.Batch, rank: int, world: int) -> dict | None:
     total_ms = sum(step_ms)
     total_ms = max_over_ranks(total_ms, device="cuda")
 
+    roof = attention_entry(cfg, b, attn_ms, peaks, peak_note, args.paged, None)
+    res = {
+        "metric": METRIC,
+        "value": world * counts["kv_bytes"] * args.steps / (total_ms / 1e3) / 1e9,
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": total_ms / args.steps,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": describe(cfg, b.ctx_lens, args.paged, world),
+        "tflops": world * counts["flops"] * args.steps / (total_ms / 1e3) / 1e12,
+        "attention_ms": statistics.mean(attn_ms),
+        "append_ms": statistics.mean(s - a for s, a in zip(step_ms, attn_ms)),
+        "roofline": roof,
+        "gpu_launches": st.launches_per_step() * args.steps,
+        "clocks": clk,
+        "plan": st.plan,
+    }
+    if args.step_only:
+        return res
+
     # ---- end to end through the public API with host buffers (pinned), copies timed: the step's
     # host inputs sit in one pinned buffer and go to the device in one copy (staging.HostStaging)
     from speculative_decoding_draft_rmsnorm_gb300.staging import HostStaging
@@ -512,36 +538,11 @@ def run_gpu(args, b: W.Batch, rank: int, world: int) -> dict | None:
     e2e_ms = sum(e[0].elapsed_time(e[1]) for e in eev)
     st.seq_lens = device_lens
 
-    ops = time_draft_ops(lib, b, flush, stream, args.steps)
-    store = time_context_store(lib, b, st, flush, stream, args.steps, peaks, peak_note)
-    roof = attention_entry(cfg, b, attn_ms, peaks, peak_note, args.paged, None)
-    res = {
-        "metric": METRIC,
-        "value": world * counts["kv_bytes"] * args.steps / (total_ms / 1e3) / 1e9,
-        "unit": "GB/s",
-        "n_gpus": world,
-        "steps": args.steps,
-        "warmup": args.warmup,
-        "ms_per_step": total_ms / args.steps,
-        "higher_is_better": True,
-        "scaling": "weak",
-        "vs_baseline": None,
-        "dtype": "bf16",
-        "data": "synthetic",
-        "config": describe(cfg, b.ctx_lens, args.paged, world),
-        "tflops": world * counts["flops"] * args.steps / (total_ms / 1e3) / 1e12,
-        "attention_ms": statistics.mean(attn_ms),
-        "append_ms": statistics.mean(s - a for s, a in zip(step_ms, attn_ms)),
-        "roofline": roof,
-        "e2e": {"value": world * counts["kv_bytes"] * args.steps / (e2e_ms / 1e3) / 1e9, "unit": "GB/s",
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "host_inputs": "one pinned staging buffer, one host-to-device copy per step"},
-        "gpu_launches": st.launches_per_step() * args.steps,
-        "clocks": clk,
-        "plan": st.plan,
-        "context_store": store,
-        "draft_step_ops": ops,
-    }
+    res["e2e"] = {"value": world * counts["kv_bytes"] * args.steps / (e2e_ms / 1e3) / 1e9, "unit": "GB/s",
+                  "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                  "host_inputs": "one pinned staging buffer, one host-to-device copy per step"}
+    res["context_store"] = time_context_store(lib, b, st, flush, stream, args.steps, peaks, peak_note)
+    res["draft_step_ops"] = time_draft_ops(lib, b, flush, stream, args.steps)
     del st, staging
     torch.cuda.empty_cache()
     # ---- the other long-context workloads of the target (Qwen3-4B-shaped and SWA layers),
@@ -732,11 +733,17 @@ def main() -> int:
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-per-workload", action="store_true",
                     help="skip timing the other long-context workloads beside the main one")
+    ap.add_argument("--step-only", action="store_true",
+                    help="time the step alone: no end-to-end, context-store, draft-op, per-workload or CPU lines "
+                         "(for profiling: fewer launches and allocations)")
     ap.add_argument("--clock-window", type=float, default=0.3,
                     help="seconds of repeated steps after the timed ones, sampled for the clock record")
     ap.add_argument("--paged", type=int, default=0, choices=[0, 16, 32, 64, 128],
                     help="context in a page pool of this many rows per page (shuffled page order); 0: contiguous")
     args = ap.parse_args()
+    if args.step_only:
+        args.no_per_workload = args.no_cpu_baseline = True
+        args.clock_window = 0.0
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     cfg = W.CONFIGS[args.workload]
