@@ -1056,23 +1056,19 @@ attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         const int col0 = 64 * half;
         const int jbase = ti.j0 + col0;
         const bool full_tile = ti.valid == kTileKeys && ti.j0 >= jlo && ti.j0 + kTileKeys - 1 <= jhi;
-        float mt = -INFINITY;
-        float x[64];
-        if (full_tile) {
+        // the running maximum is taken over the raw scores (the scale is positive); masked keys
+        // become -inf in place
+        float* x = reinterpret_cast<float*>(sr);
+        if (!full_tile) {
+          const int c_lo = max(jlo - jbase, 0);
+          const int c_hi = min(jhi - jbase, ti.valid - col0 - 1);
 #pragma unroll
-          for (int c = 0; c < 64; ++c) {
-            x[c] = __uint_as_float(sr[c]) * sl2;
-            mt = fmaxf(mt, x[c]);
-          }
-        } else {
-#pragma unroll
-          for (int c = 0; c < 64; ++c) {
-            const int jj = jbase + c;
-            const bool keep = (col0 + c < ti.valid) && jj >= jlo && jj <= jhi;
-            x[c] = keep ? __uint_as_float(sr[c]) * sl2 : -INFINITY;
-            mt = fmaxf(mt, x[c]);
-          }
+          for (int c = 0; c < 64; ++c) x[c] = (c >= c_lo && c <= c_hi) ? x[c] : -INFINITY;
         }
+        float mt = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < 64; c += 2) mt = fmax3(mt, x[c], x[c + 1]);
+        mt *= sl2;
         mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 16));
         float alpha = 1.0f;
         bool rescale = false;
@@ -1103,24 +1099,32 @@ attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
           tmem_wait_st();
         }
         const float m_eff = m_used == -INFINITY ? 0.0f : m_used;
+        // exponent s * scale - m for two keys per instruction; the weight sums two lanes wide
+        const uint64_t sl2x2 = f32x2(sl2, sl2), negm = f32x2(-m_eff, -m_eff);
         uint32_t pk[32];
         uint32_t pl[PRECISE ? 32 : 1];
-        float lsum = 0.0f;
+        uint64_t lsum2 = f32x2(0.0f, 0.0f);
 #pragma unroll
         for (int c = 0; c < 64; c += 2) {
-          const float p0 = ex2_approx(x[c] - m_eff);
-          const float p1 = ex2_approx(x[c + 1] - m_eff);
+          float a0, a1;
+          f32x2_split(fma_f32x2(f32x2(x[c], x[c + 1]), sl2x2, negm), a0, a1);
+          const float p0 = ex2_approx(a0);
+          const float p1 = ex2_approx(a1);
           const uint32_t v = pack_bf16x2(p0, p1);
           pk[c / 2] = v;
           if (PRECISE) {
             // P = P_hi + P_lo; l sums the unrounded weights
             pl[c / 2] = pack_bf16x2(p0 - bf16lo_to_f32(v), p1 - bf16hi_to_f32(v));
-            lsum += p0 + p1;
+            lsum2 = add_f32x2(lsum2, f32x2(p0, p1));
           } else {
-            lsum += bf16lo_to_f32(v) + bf16hi_to_f32(v);  // l sums exactly the weights PV uses
+            lsum2 = add_f32x2(lsum2, f32x2(bf16lo_to_f32(v), bf16hi_to_f32(v)));  // exactly the weights PV uses
           }
         }
-        l += lsum;
+        {
+          float s0, s1;
+          f32x2_split(lsum2, s0, s1);
+          l += s0 + s1;
+        }
         // the P buffer is free once PV of tile g-2 has completed
         if (!(ok = wait_warp(bar(L::P_EMPTY + sb), ((g >> 1) & 1) ^ 1))) break;
         {
