@@ -52,7 +52,9 @@ def _oracle_paged(b: W.Batch, kp, vp, bt, page_size, **kw):
 CASES = [
     ("qwen3_0p6b", 16, {}),
     ("qwen3_0p6b", 64, {}),
+    ("qwen3_0p6b", 128, {}),                  # one box brings a whole 128-key tile
     ("swa_small", 16, {}),                    # window start not on a page boundary
+    ("swa_small", 128, {}),
     ("tiny", 16, {}),
     ("ragged_small", 32, {}),
 ]
@@ -76,14 +78,15 @@ def test_paged_matches_oracle_bf16(name, page_size, kw):
     U.assert_close_bf16(got, _oracle_paged(b, kp, vp, bt, page_size), f"{name} ps={page_size}")
 
 
-@pytest.mark.parametrize("name", ["qwen3_0p6b", "swa_small", "tiny"])
-def test_paged_matches_oracle_f32(name):
+@pytest.mark.parametrize("name,page_size", [("qwen3_0p6b", 16), ("swa_small", 16), ("tiny", 16),
+                                            ("ragged_small", 32), ("swa_small", 128)])
+def test_paged_matches_oracle_f32(name, page_size):
     cfg = _cfg(name)
     b = W.make_batch(cfg)
     ck = U.stored_ctx_k(b)
-    kp, vp, bt = _paged_inputs(b, ck, 16)
-    got = U.dev_to_f64(_gpu_paged(b, kp, vp, bt, out_dtype=1))
-    U.assert_close_f32(got, _oracle_paged(b, kp, vp, bt, 16), f"{name} f32")
+    kp, vp, bt = _paged_inputs(b, ck, page_size)
+    got = U.dev_to_f64(_gpu_paged(b, kp, vp, bt, out_dtype=1, flags=1 if cfg.force_split else 0))
+    U.assert_close_f32(got, _oracle_paged(b, kp, vp, bt, page_size), f"{name} ps={page_size} f32")
 
 
 @pytest.mark.parametrize("flags", [0, 1, 2])
