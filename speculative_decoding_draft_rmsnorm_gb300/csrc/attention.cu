@@ -358,6 +358,15 @@ __global__ void __launch_bounds__(256, 3) prologue_kernel(const __grid_constant_
 }
 
 // ================================================================ kernel B
+// With two Q buffers (bf16 output), a whole group's normalised rows go out through the
+// segment's own Q buffer: each thread holds 64 columns of one row, which written straight to
+// global memory scatters every 16-byte store over 32 rows; staged, each half-warp writes a full
+// row. The buffer is free once the segment's O_FULL has landed (its last QK completed), and the
+// producer reloads it (two segments later) only after the softmax warps have arrived on Q_EMPTY.
+// With one Q buffer the next segment's Q would wait on this epilogue, which itself waits for the
+// next segment's first tile, so that configuration stores directly.
+template <int NQ, bool PRECISE>
+constexpr bool kStagedOut = NQ >= 2 && !PRECISE;
 // A partial slot (64 rows x DH f32) is stored in the order the softmax threads hold it: the
 // thread of TMEM sub-partition sp and lane L (row 16 sp + L % 16, columns from (L / 16) DH / 2)
 // writes its k-th 4-float group (columns + 4k .. 4k + 3) at float4 index
@@ -659,7 +668,9 @@ attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar(L::Q_FULL + i), 1);
-      mbar_init(bar(L::Q_EMPTY + i), 1);
+      // the MMA's last QK of the segment, and (staged epilogue) the four softmax warps once the
+      // segment's output has left the buffer
+      mbar_init(bar(L::Q_EMPTY + i), kStagedOut<NQ, PRECISE> ? 5 : 1);
       mbar_init(bar(L::S_FULL + i), 1);
       mbar_init(bar(L::S_EMPTY + i), 4);
       mbar_init(bar(L::P_FULL + i), 4);
@@ -965,8 +976,41 @@ attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(L::O_EMPTY + (e_iu & 1)));
       const float l_tot = e.l + __shfl_xor_sync(0xffffffffu, e.l, 16);
-      if (!(e.state & 2)) return true;
-      if (e.state & 4) {
+      const bool row_ok = (e.state & 2) != 0;
+      if ((e.state & 4) && kStagedOut<NQ, PRECISE>) {
+        // bf16 rows through the segment's Q buffer, 128-byte swizzled: this warp's 16 rows at
+        // sp * 16 rows; 16-byte chunk k of row r at chunk position k ^ (r & 7)
+        const float inv = l_tot > 0.0f ? 1.0f / l_tot : 0.0f;
+        constexpr int CPRW = DH * 2 / 16;  // 16-byte chunks per row
+        uint8_t* stg = smem + L::OFF_Q + (e_iu % NQ) * L::QBT + sp * (16 * DH * 2);
+        const int r16 = lane & 15;
+#pragma unroll
+        for (int ch = 0; ch < CH; ++ch)
+#pragma unroll
+          for (int x = 0; x < 32; x += 8) {
+            uint4 v;
+            v.x = pack_bf16x2(__uint_as_float(o[ch][x]) * inv, __uint_as_float(o[ch][x + 1]) * inv);
+            v.y = pack_bf16x2(__uint_as_float(o[ch][x + 2]) * inv, __uint_as_float(o[ch][x + 3]) * inv);
+            v.z = pack_bf16x2(__uint_as_float(o[ch][x + 4]) * inv, __uint_as_float(o[ch][x + 5]) * inv);
+            v.w = pack_bf16x2(__uint_as_float(o[ch][x + 6]) * inv, __uint_as_float(o[ch][x + 7]) * inv);
+            const int k = half * (CPRW / 2) + ch * 4 + x / 8;
+            *reinterpret_cast<uint4*>(stg + r16 * (DH * 2) + ((k ^ (r16 & 7)) << 4)) = v;
+          }
+        __syncwarp();
+        // read back a row per half-warp (two rows per step at Dh = 128, four at Dh = 64)
+        constexpr int RPI = 32 / CPRW;
+#pragma unroll
+        for (int i = 0; i < 16 / RPI; ++i) {
+          const int r = i * RPI + lane / CPRW, c = lane % CPRW;
+          const int row_g = __shfl_sync(0xffffffffu, e.row, r);
+          const int ok_r = __shfl_sync(0xffffffffu, row_ok ? 1 : 0, r);
+          const uint4 v = *reinterpret_cast<const uint4*>(stg + r * (DH * 2) + ((c ^ (r & 7)) << 4));
+          if (ok_r) *reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(p.out) + static_cast<int64_t>(row_g) * DH + c * 8) = v;
+        }
+        __syncwarp();
+      } else if (!row_ok) {
+        // no output row (a query tile's rows past its group's last token)
+      } else if (e.state & 4) {
         const float inv = l_tot > 0.0f ? 1.0f / l_tot : 0.0f;
         if (p.out_f32) {
           float* dst = reinterpret_cast<float*>(p.out) + static_cast<int64_t>(e.row) * DH + half * (DH / 2);
@@ -1009,6 +1053,7 @@ attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         if (half == 0)
           st_global_v2_hint(p.part_ml + (static_cast<int64_t>(pslot) * kTileRows + rho) * 2, e.m, l_tot, pol_keep);
       }
+      if (kStagedOut<NQ, PRECISE> && lane == 0) mbar_arrive(bar(L::Q_EMPTY + (e_iu % NQ)));
       return true;
     };
     // One pass per segment, plus a last one without tiles for the last segment's epilogue, so
