@@ -27,10 +27,11 @@
 //   C  combine: merges the partials of each group that straddles CTAs:
 //      o = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s.
 //
-// TMEM map (512 columns): S[0] at column 0, S[1] at 128, O at 256. An M = 64 MMA puts
-// query row rho in lane 32*(rho/16) + rho%16; softmax warp w (sub-partition w%4) owns
-// rows 16*(w%4) .. +15, lanes 0-15 of the warp taking key columns 0-63 and lanes
-// 16-31 columns 64-127 (tcgen05.ld 16x32bx2).
+// TMEM map (512 columns): S[0] at column 0, S[1] at 128, O of even segments at 256 and of
+// odd segments at 256 + Dh (a segment's first PV waits only for the epilogue two segments
+// back). An M = 64 MMA puts query row rho in lane 32*(rho/16) + rho%16; softmax warp w
+// (sub-partition w%4) owns rows 16*(w%4) .. +15, lanes 0-15 of the warp taking key columns
+// 0-63 and lanes 16-31 columns 64-127 (tcgen05.ld 16x32bx2).
 #include <algorithm>
 #include <cmath>
 #include <cstdio>
