@@ -137,6 +137,7 @@ SMALL_CASES = [
     ("g16", 32, 2, 128, False, 0, [700, 5, 260], [16, 7, 16]),    # 4 tokens a query tile
     ("g32_causal", 64, 2, 64, True, 0, [300, 129], [16, 3]),       # 2 tokens a query tile
     ("mqa_g64", 64, 1, 128, True, 100, [500, 0, 64], [16, 9, 5]),  # one kv head, 1 token a query tile
+    ("long_blocks", 8, 2, 128, True, 0, [900, 40], [150, 130]),    # 2 block-key tiles (3 in f32), 10 query tiles
 ]
 
 
@@ -151,7 +152,8 @@ def test_block_attention_small_bf16(case):
 
 
 F32_CASES = [c for c in SMALL_CASES if c[0] in ("tiny_cfg", "gqa4_dh128", "no_context", "ragged_blocks", "causal",
-                                               "swa", "swa_w1", "two_qtiles", "g8_qtiles", "mqa_g64")]
+                                               "swa", "swa_w1", "two_qtiles", "g8_qtiles", "mqa_g64",
+                                               "long_blocks")]
 
 
 @pytest.mark.parametrize("case", F32_CASES, ids=[c[0] for c in F32_CASES])
