@@ -6,8 +6,9 @@ workload at its full size, and every output element is compared with the oracle:
 output within max|diff| 1.5e-2 and mean|diff| 2e-3 (end to end: the GPU-built store
 against the oracle's exact context keys), f32 output within 2e-4 (both sides given the
 same stored bf16 keys, so the comparison isolates the attention). The paged call with
-16-row pages (the pages' own page size) runs on the Qwen3-4B-shaped layer in both output
-types. The oracle of each workload is computed once per module and reused.
+16-row pages (the pages' own page size) runs on the Qwen3-4B-shaped and the sliding-window
+layers in both output types. The oracle of each workload is computed once per module
+and reused.
 """
 from __future__ import annotations
 
@@ -73,25 +74,29 @@ def test_full_size_every_row_f32(name):
 
 
 @pytest.mark.parametrize("out_dtype", [0, 1])
-def test_full_size_paged_16_row_pages(out_dtype):
-    # the Qwen3-4B-shaped layer with its context in 16-row pages handed out in shuffled order
+@pytest.mark.parametrize("name", ["qwen3_4b", "swa"])
+def test_full_size_paged_16_row_pages(name, out_dtype):
+    # the layer with its context in 16-row pages handed out in shuffled order (for the sliding
+    # window, its first context tile starts on the page boundary below the window's first key)
     import torch
-    b, ck, want_contig = _case("qwen3_4b")
+    b, ck, want_contig = _case(name)
     c, ps = b.cfg, 16
     order = np.random.default_rng(5).permutation(sum((int(l) + ps - 1) // ps for l in b.ctx_lens))
     pool_k, bt = U.to_pages(ck, b.ctx_start_loc, b.ctx_lens, ps, order)
     pool_v, _ = U.to_pages(b.ctx_v, b.ctx_start_loc, b.ctx_lens, ps, order)
     want = oracle.block_attention_paged(b.q, b.k_blk, b.v_blk, pool_k, pool_v, bt, b.query_start_loc, b.ctx_lens,
-                                        b.positions, b.q_norm_w, b.k_norm_w, ps, eps=c.eps, theta=c.theta)
+                                        b.positions, b.q_norm_w, b.k_norm_w, ps, eps=c.eps, theta=c.theta,
+                                        causal=c.causal, window=c.window)
     assert np.array_equal(want, want_contig)  # the paged oracle is the contiguous one on gathered rows
     out = D().block_attention_paged(U.bf16_dev(b.q), U.bf16_dev(b.k_blk), U.bf16_dev(b.v_blk), U.bf16_dev(pool_k),
                                     U.bf16_dev(pool_v), U.i32_dev(bt), U.i32_dev(b.query_start_loc),
                                     U.i32_dev(b.ctx_lens), U.i32_dev(b.positions), U.bf16_dev(b.q_norm_w),
                                     U.bf16_dev(b.k_norm_w), max_ctx_len=int(b.ctx_lens.max()), max_block_len=c.block,
-                                    eps=c.eps, theta=c.theta, out_dtype=out_dtype)
+                                    eps=c.eps, theta=c.theta, causal=c.causal, window=c.window,
+                                    out_dtype=out_dtype)
     torch.cuda.synchronize()
     got = U.dev_to_f64(out)
     if out_dtype:
-        U.assert_close_f32(got, want, "qwen3_4b paged16 f32")
+        U.assert_close_f32(got, want, f"{name} paged16 f32")
     else:
-        U.assert_close_bf16(got, want, "qwen3_4b paged16 bf16")
+        U.assert_close_bf16(got, want, f"{name} paged16 bf16")
